@@ -1,0 +1,61 @@
+// kernels.h -- internal launchers of the CUDA library (host side).  The public
+// C ABI lives in include/fp8moe.h; these are the per-file entry points that
+// api.cu calls after validating arguments and building tensor maps.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const int32_t* gs,
+                                        int E, uint8_t* q, float* sx, int num_sms, int report,
+                                        cudaStream_t s);
+cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
+                                              int N, const int32_t* gs, int E, int64_t Smax,
+                                              uint8_t* qx, float* sx, uint8_t* qd, float* sd,
+                                              int num_sms, int report, cudaStream_t s);
+cudaError_t fp8moe_launch_dequantize(const uint8_t* codes, const float* scale, int E, int64_t K,
+                                     int64_t N, void* out, int num_sms, cudaStream_t s);
+
+// Forward grouped matmul (FP8 x FP8 or the BF16 comparison arm).
+struct GmmFwdArgs {
+  CUtensorMap tmA;        // A operand tiles (codes [M, K] u8, or lhs [M, K] bf16)
+  CUtensorMap tmB;        // B operand tiles (weights [E, K, N], N contiguous)
+  const float* sx;        // [M] row scales (FP8 arm) or nullptr
+  const float* scale;     // [E, N] channel scales (FP8 arm) or nullptr
+  const int32_t* gs;      // [E]
+  void* out;              // bf16 [M, Nout]
+  int64_t M;
+  int K, N, E, swiglu;
+};
+cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);
+cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);
+
+struct GmmDlhsArgs {
+  CUtensorMap tmA;        // dout [M, N] bf16 tiles
+  CUtensorMap tmC;        // codes [E, K, N] u8 tiles
+  const float* scale;     // [E, N]
+  const int32_t* gs;
+  void* dlhs;             // bf16 [M, K]
+  int64_t M;
+  int N, K, E;
+};
+cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int cached,
+                                   cudaStream_t s);
+
+struct TgmmArgs {
+  CUtensorMap tmX;        // qx slots [S, 128, K] u8
+  CUtensorMap tmD;        // qd slots [S, 128, N] u8
+  const float* sx;        // [S, K]
+  const float* sd;        // [S, N]
+  const int32_t* gs;
+  float* dW;              // [E, K, N]
+  int64_t M;
+  int K, N, E;
+};
+cudaError_t fp8moe_launch_tgmm(const TgmmArgs& a, int num_sms, cudaStream_t s);
+
+uint32_t fp8moe_status_take_quant(cudaStream_t s);
+uint32_t fp8moe_status_take_dequant(cudaStream_t s);
+uint32_t fp8moe_status_take_gmm_fwd(cudaStream_t s);
+uint32_t fp8moe_status_take_dlhs(cudaStream_t s);
+uint32_t fp8moe_status_take_tgmm(cudaStream_t s);

@@ -1,0 +1,263 @@
+// quant.cu -- activation quantization kernels.
+//
+//  * quantize_rows_kernel: the forward GMM's A operand. One f32 absmax scale per
+//    row over the whole K, scale = max(amax, 1e-12) / 448, codes = e4m3(x / scale)
+//    ("MoE: native FP8 QAT for routed-expert GMMs", Description and
+//    Implementation: in-kernel full-K activation quantization with an f32 scale).
+//    One warp per row, the row held in registers between the amax pass and the
+//    cast pass; rows at or past T = sum(group_sizes) are never read.
+//
+//  * tgmm_quantize_tiles_kernel: the weight-gradient operands, per 128-row tile
+//    and per channel, over the rows of one group only ("MoE fp8 backward:
+//    in-kernel drhs operand quantization", What). Codes go to 128-row slots, one
+//    per (tile, group) segment, rows outside the segment zeroed, so the
+//    contraction kernel can TMA whole slots without masking.
+//
+// Both divide with IEEE round-to-nearest (this file is compiled without fast
+// math) and cast with cvt.rn.satfinite, so codes and scales are bit-exact with a
+// plain f32 reading of the definition.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "groups.cuh"
+#include "kernels.h"
+
+namespace fp8moe {
+
+constexpr float kEps = 1e-12f;
+constexpr float kE4m3Max = 448.0f;
+
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t v) {
+  uint32_t a = v & 0x7FFF7FFFu, r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t v) {
+  return fmaxf(bf16lo_to_f32(v), bf16hi_to_f32(v));
+}
+
+// 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2).
+__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
+  uint2 o;
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint16_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo = __fdiv_rn(bf16lo_to_f32(w[i]), s);
+    float hi = __fdiv_rn(bf16hi_to_f32(w[i]), s);
+    c[i] = f32x2_to_e4m3x2(lo, hi);
+  }
+  o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+  o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+  return o;
+}
+
+// ------------------------------------------------------------------------ a1
+// One warp per row; each lane holds up to MAXC 16-byte chunks of the row.
+template <int MAXC>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(
+    const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
+    int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
+  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
+  __shared__ int32_t s_T;
+  load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
+  __syncthreads();
+  const int T = s_T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = K >> 3;   // K % 8 == 0
+  const int warps_total = gridDim.x * 8;
+  for (int64_t m = (int64_t)blockIdx.x * 8 + warp; m < T; m += warps_total) {
+    const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
+    uint4 v[MAXC];
+    uint32_t amax2 = 0;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      int c = lane + 32 * i;
+      if (c < nchunk) {
+        v[i] = __ldg(row + c);
+        amax2 = bf16x2_absmax(amax2, v[i].x);
+        amax2 = bf16x2_absmax(amax2, v[i].y);
+        amax2 = bf16x2_absmax(amax2, v[i].z);
+        amax2 = bf16x2_absmax(amax2, v[i].w);
+      }
+    }
+    float amax = bf16x2_hmax_to_f32(amax2);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
+    uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      int c = lane + 32 * i;
+      if (c < nchunk) qrow[c] = quant8(v[i], s);
+    }
+    if (lane == 0) sx[m] = s;
+  }
+}
+
+// Rows longer than the register cache: the cast pass re-reads the row (L2 hit).
+__global__ void __launch_bounds__(256) quantize_rows_stream_kernel(
+    const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
+    int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
+  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
+  __shared__ int32_t s_T;
+  load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
+  __syncthreads();
+  const int T = s_T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = K >> 3;
+  const int warps_total = gridDim.x * 8;
+  for (int64_t m = (int64_t)blockIdx.x * 8 + warp; m < T; m += warps_total) {
+    const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
+    uint32_t amax2 = 0;
+    for (int c = lane; c < nchunk; c += 32) {
+      uint4 v = __ldg(row + c);
+      amax2 = bf16x2_absmax(amax2, v.x);
+      amax2 = bf16x2_absmax(amax2, v.y);
+      amax2 = bf16x2_absmax(amax2, v.z);
+      amax2 = bf16x2_absmax(amax2, v.w);
+    }
+    float amax = bf16x2_hmax_to_f32(amax2);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
+    uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+    for (int c = lane; c < nchunk; c += 32) qrow[c] = quant8(__ldg(row + c), s);
+    if (lane == 0) sx[m] = s;
+  }
+}
+
+// ------------------------------------------------------------------------ a7
+// Segment table: nseg[e] = number of 128-row tiles touched by group e, seg_base =
+// exclusive prefix (segments numbered expert by expert, tiles ascending).
+__device__ __forceinline__ void build_segments_warp0(const int32_t* s_begin, const int32_t* s_end,
+                                                     int E, int32_t* s_segbase) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int32_t carry = 0;
+  for (int base = 0; base < E; base += 32) {
+    int e = base + lane;
+    int32_t n = 0;
+    if (e < E && s_end[e] > s_begin[e]) n = (s_end[e] - 1) / 128 - s_begin[e] / 128 + 1;
+    int32_t incl = n;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    if (e < E) s_segbase[e] = carry + incl - n;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) s_segbase[E] = carry;
+}
+
+// Work unit = (segment, 2048-column chunk) over the columns of lhs then dout.
+// Each warp owns 256 columns (8 per lane).
+__global__ void __launch_bounds__(256) tgmm_quantize_tiles_kernel(
+    const __nv_bfloat16* __restrict__ lhs, const __nv_bfloat16* __restrict__ dout, int64_t M,
+    int K, int N, const int32_t* __restrict__ gs, int E, int64_t Smax,
+    uint8_t* __restrict__ qx, float* __restrict__ sx, uint8_t* __restrict__ qd,
+    float* __restrict__ sd, int report) {
+  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts], s_segbase[kMaxExperts + 1];
+  __shared__ int32_t s_T;
+  load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
+  __syncthreads();
+  build_segments_warp0(s_begin, s_end, E, s_segbase);
+  __syncthreads();
+  const int S = s_segbase[E];
+  if (S > Smax) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(kStatusTooManySegments);
+    return;
+  }
+  const int ck = (K + 2047) / 2048, cn = (N + 2047) / 2048, cpq = ck + cn;
+  const int64_t units = (int64_t)S * cpq;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int qi = (int)(u / cpq), ch = (int)(u % cpq);
+    const int e = find_bucket(s_segbase, E, qi);
+    const int t = s_begin[e] / 128 + (qi - s_segbase[e]);
+    const int r0 = max(s_begin[e], t * 128), r1 = min(s_end[e], t * 128 + 128);
+    const bool is_x = ch < ck;
+    const int C = is_x ? K : N;
+    const int c0 = (is_x ? ch : ch - ck) * 2048 + warp * 256 + lane * 8;
+    if (c0 >= C) continue;
+    const __nv_bfloat16* src = is_x ? lhs : dout;
+    uint8_t* qo = (is_x ? qx : qd) + (int64_t)qi * 128 * C;
+    float* so = (is_x ? sx : sd) + (int64_t)qi * C;
+    // pass 1: per-column absmax over the segment rows
+    uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+    for (int m = r0; m < r1; ++m) {
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)m * C + c0));
+      a0 = bf16x2_absmax(a0, v.x);
+      a1 = bf16x2_absmax(a1, v.y);
+      a2 = bf16x2_absmax(a2, v.z);
+      a3 = bf16x2_absmax(a3, v.w);
+    }
+    float s[8];
+    const uint32_t aw[4] = {a0, a1, a2, a3};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s[2 * i] = __fdiv_rn(fmaxf(bf16lo_to_f32(aw[i]), kEps), kE4m3Max);
+      s[2 * i + 1] = __fdiv_rn(fmaxf(bf16hi_to_f32(aw[i]), kEps), kE4m3Max);
+    }
+    reinterpret_cast<float4*>(so + c0)[0] = make_float4(s[0], s[1], s[2], s[3]);
+    reinterpret_cast<float4*>(so + c0)[1] = make_float4(s[4], s[5], s[6], s[7]);
+    // pass 2: codes into the slot; slot rows outside the segment are zero
+    for (int r = 0; r < 128; ++r) {
+      const int m = t * 128 + r;
+      uint2 o = make_uint2(0u, 0u);
+      if (m >= r0 && m < r1) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)m * C + c0));
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint16_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          c[i] = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_to_f32(w[i]), s[2 * i]),
+                                 __fdiv_rn(bf16hi_to_f32(w[i]), s[2 * i + 1]));
+        o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+        o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+      }
+      *reinterpret_cast<uint2*>(qo + (int64_t)r * C + c0) = o;
+    }
+  }
+}
+
+}  // namespace fp8moe
+
+FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_quant)
+
+// ------------------------------------------------------------------ launchers
+cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const int32_t* gs,
+                                        int E, uint8_t* q, float* sx, int num_sms, int report,
+                                        cudaStream_t s) {
+  using namespace fp8moe;
+  int64_t blocks_needed = (M + 7) / 8;
+  int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
+  if (grid < 1) grid = 1;
+  const auto* x = static_cast<const __nv_bfloat16*>(lhs);
+  const int nchunk_lane = (K / 8 + 31) / 32;
+  if (nchunk_lane <= 8)
+    quantize_rows_kernel<8><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  else if (nchunk_lane <= 16)
+    quantize_rows_kernel<16><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  else if (nchunk_lane <= 32)
+    quantize_rows_kernel<32><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  else
+    quantize_rows_stream_kernel<<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  return cudaGetLastError();
+}
+
+cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
+                                              int N, const int32_t* gs, int E, int64_t Smax,
+                                              uint8_t* qx, float* sx, uint8_t* qd, float* sd,
+                                              int num_sms, int report, cudaStream_t s) {
+  using namespace fp8moe;
+  int grid = num_sms * 8;
+  tgmm_quantize_tiles_kernel<<<grid, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(lhs), static_cast<const __nv_bfloat16*>(dout), M, K, N,
+      gs, E, Smax, qx, sx, qd, sd, report);
+  return cudaGetLastError();
+}

@@ -1,0 +1,226 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the same
+seeded inputs, at sizes that span several tiles and ragged tails, plus the edge
+cases (empty groups, all groups empty, tail garbage, sizes that are not tile
+multiples)."""
+import pytest
+import torch
+
+from fp8_moe_routed_gb300 import binding as fb
+from fp8_moe_routed_gb300 import workloads as W
+from parity_util import bits16, check_bf16, check_f32_rel
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def cuda(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fb.load()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    fb.read_status()
+    yield
+    assert fb.read_status() == 0
+
+
+# ------------------------------------------------------------------ dequant
+def test_dequantize_all_codes_bit_exact(orc):
+    E, K, N = 3, 512, 256
+    g = torch.Generator().manual_seed(5)
+    codes = (torch.arange(E * K * N) * 7 + 3).remainder(256).to(torch.uint8).view(E, K, N)
+    codes[(codes & 0x7F) == 0x7F] = 0x11       # NaN codes are not weights
+    scale = torch.exp(torch.randn(E, N, generator=g) * 3).float()
+    out = fb.dequantize_fp8_codes(*cuda(codes, scale))
+    ref = orc.dequantize(codes, scale)
+    assert torch.equal(bits16(out), bits16(ref))
+
+
+@pytest.mark.parametrize("E,K,N", [(4, 256, 256), (2, 7168, 64), (5, 48, 4096)])
+def test_dequantize_shapes(orc, E, K, N):
+    codes, scale = W.fp8_weights(E, K, N, 0.01, seed=E + K)
+    out = fb.dequantize_fp8_codes(*cuda(codes, scale))
+    assert torch.equal(bits16(out), bits16(orc.dequantize(codes, scale)))
+
+
+# ------------------------------------------------------------- row quantize
+@pytest.mark.parametrize("M,K,gs", [
+    (512, 256, None), (300, 2048, [100, 0, 150, 20]), (200, 7168, [64, 64, 0, 60]),
+    (64, 9216, [40, 24]), (130, 16, [129, 1]),
+])
+def test_quantize_rows_bit_exact(orc, M, K, gs):
+    gs = W.group_sizes("tiny", seed=1, M=M) if gs is None else torch.tensor(gs, dtype=torch.int32)
+    x = W.activations(M, K, seed=K, outlier_frac=0.05)
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(x, T)
+    x[0, :] = 0                         # zero row -> scale 1e-12/448
+    q, sx = fb.quantize_rows(*cuda(x, gs))
+    q_ref, sx_ref, bad = orc.quantize_rows(x, gs)
+    assert bad == 0
+    assert torch.equal(q.cpu()[:T], q_ref[:T])
+    assert torch.equal(sx.cpu()[:T], sx_ref[:T])
+    assert (q.cpu()[T:] == 0).all() and torch.isnan(sx.cpu()[T:]).all()   # untouched
+
+
+# ------------------------------------------------------------ forward GMM
+def fwd_case(M, K, N, E, gs, seed, outliers=0.0, tail_garbage=True):
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    x = W.activations(M, K, seed, outlier_frac=outliers)
+    if tail_garbage:
+        x = W.fill_tail_garbage(x, int(gs.sum()))
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed + 1)
+    return x, codes, scale, gs
+
+
+FWD_CASES = [
+    # M, K, N, E, group sizes
+    (512, 256, 256, 4, "tiny"),
+    (700, 512, 512, 5, [300, 0, 129, 1, 200]),      # T=630 < M: ragged tail
+    (384, 1024, 768, 3, [0, 384, 0]),               # one group owns everything
+    (256, 256, 352, 2, [100, 100]),                 # N not a multiple of 256 (silu: 176)
+]
+
+
+@pytest.mark.parametrize("silu", [True, False])
+@pytest.mark.parametrize("M,K,N,E,gs", FWD_CASES)
+def test_gmm_fwd_vs_oracle(orc, M, K, N, E, gs, silu):
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=0, M=M, E=E)
+    x, codes, scale, gs = fwd_case(M, K, N, E, gs, seed=M + N, outliers=0.01)
+    T = int(gs.sum())
+    Nout = N // 2 if silu else N
+    out = torch.full((M, Nout), 7.0, dtype=torch.bfloat16, device=DEV)   # sentinel
+    fn = fb.gmm_silu_fp8_fwd if silu else fb.gmm_fp8_fwd
+    fn(*cuda(x, codes, scale, gs), out=out)
+    ref, _, bad = orc.gmm_fwd(x, codes, scale, gs, silu=silu)
+    assert bad == 0
+    check_bf16(out[:T], ref[:T], what=f"fwd silu={silu}")
+    assert (out[T:].float() == 7.0).all(), "rows >= T were written"
+
+
+def test_gmm_fwd_all_groups_empty():
+    M, K, N, E = 256, 256, 256, 4
+    x, codes, scale, gs = fwd_case(M, K, N, E, [0, 0, 0, 0], seed=3)
+    out = torch.full((M, N // 2), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_silu_fp8_fwd(*cuda(x, codes, scale, gs), out=out)
+    assert (out.float() == 7.0).all()
+
+
+def test_gmm_fwd_lossless_rows_equal_plain_matmul():
+    """Rows on the e4m3 grid with amax 448: quantization is exact, the FP8 GMM
+    equals the float64 matmul with the dequantized weight (to one rounding)."""
+    M, K, N, E = 256, 512, 256, 2
+    g = torch.Generator().manual_seed(4)
+    cx = torch.randint(0, 256, (M, K), generator=g, dtype=torch.uint8)
+    cx[(cx & 0x7F) == 0x7F] = 0x30
+    cx[:, 0] = 0x7E
+    x = cx.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    codes, scale = W.fp8_weights(E, K, N, 0.05, 9)
+    gs = torch.tensor([100, 156], dtype=torch.int32)
+    out = fb.gmm_fp8_fwd(*cuda(x, codes, scale, gs))
+    w = codes.view(torch.float8_e4m3fn).double() * scale.double()[:, None, :]
+    ref = torch.cat([x[:100].double() @ w[0], x[100:].double() @ w[1]])
+    check_bf16(out, ref, what="lossless")
+
+
+# ------------------------------------------------------------------- dLHS
+DLHS_CASES = [
+    (512, 256, 256, 4, "tiny"),                      # contraction 256: cached path
+    (700, 512, 512, 5, [300, 0, 129, 1, 200]),       # streaming
+    (300, 2048, 256, 3, [0, 280, 20]),
+    (260, 512, 1088, 2, [130, 100]),                 # K-out not a multiple of 256
+]
+
+
+@pytest.mark.parametrize("M,N,K,E,gs", DLHS_CASES)
+def test_dlhs_vs_oracle_and_paths_identical(orc, M, N, K, E, gs):
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=0, M=M, E=E)
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    T = int(gs.sum())
+    dout = W.fill_tail_garbage(W.cotangent(M, N, seed=N), T)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=K)
+    args = cuda(dout, codes, scale, gs)
+    out0 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out0, path=0)
+    ref, _, bad = orc.gmm_dlhs(dout, codes, scale, gs)
+    assert bad == 0
+    check_bf16(out0[:T], ref[:T], what="dlhs")
+    assert (out0[T:].float() == 7.0).all()
+    if N <= 256:
+        out1 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+        fb.gmm_dlhs_fp8(*args, out=out1, path=1)
+        assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
+
+
+# ------------------------------------------------------------------- tgmm
+TGMM_CASES = [
+    (512, 256, 256, 4, "tiny"),
+    (1024, 512, 512, 6, [300, 0, 129, 1, 200, 0]),   # T=630, tail garbage, straddles
+    (384, 256, 768, 3, [0, 0, 0]),                   # all empty: dW = 0
+]
+
+
+@pytest.mark.parametrize("M,K,N,E,gs", TGMM_CASES)
+def test_tgmm_vs_oracle(orc, M, K, N, E, gs):
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=2, M=M, E=E)
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=K), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=N), T)
+    dw = fb.tgmm_drhs_quant(*cuda(x, d, gs))
+    ref, bad = orc.tgmm(x, d, gs)
+    assert bad == 0
+    assert torch.isfinite(dw).all()
+    if T == 0:
+        assert (dw == 0).all()
+    else:
+        check_f32_rel(dw, ref, what="tgmm")
+        for e in range(E):
+            if int(gs[e]) == 0:
+                assert (dw[e] == 0).all()
+
+
+def test_tgmm_quantize_tiles_bit_exact(orc):
+    M, K, N = 1024, 512, 256
+    gs = torch.tensor([300, 0, 129, 1, 200, 0], dtype=torch.int32)
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=1), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=2), T)
+    qx, sx, qd, sd = fb.tgmm_quantize_tiles(*cuda(x, d, gs))
+    rqx, rsx, rqd, rsd, nseg, bad = orc.tgmm_quantize_tiles(x, d, gs)
+    assert bad == 0
+    assert torch.equal(qx.cpu()[:nseg], rqx[:nseg]) and torch.equal(qd.cpu()[:nseg], rqd[:nseg])
+    assert torch.equal(sx.cpu()[:nseg], rsx[:nseg]) and torch.equal(sd.cpu()[:nseg], rsd[:nseg])
+
+
+# --------------------------------------------------------- BF16 comparison
+@pytest.mark.parametrize("swiglu", [True, False])
+def test_bf16_gmm_vs_float64(orc, swiglu):
+    M, K, N, E = 640, 512, 512, 4
+    gs = torch.tensor([200, 0, 300, 100], dtype=torch.int32)
+    T = 600
+    x = W.fill_tail_garbage(W.activations(M, K, seed=8), T)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=9)
+    w = orc.dequantize(codes, scale)
+    out = fb.gmm_bf16_fwd(*cuda(x, w, gs), swiglu=swiglu)
+    xd, wd = x.double(), w.double()
+    ref = torch.zeros(M, N, dtype=torch.float64)
+    off = 0
+    for e, g in enumerate(gs.tolist()):
+        ref[off:off + g] = xd[off:off + g] @ wd[e]
+        off += g
+    if swiglu:
+        ref = torch.nn.functional.silu(ref[:, :N // 2]) * ref[:, N // 2:]
+    check_bf16(out[:T], ref[:T], what="bf16 gmm")
