@@ -38,6 +38,7 @@ import torch  # noqa: E402
 
 E, HID, FF, TOKENS, TOPK = 32, 7168, 2048, 4096, 8
 M = TOKENS * TOPK
+ROWS_PER_EXPERT = M // E
 METRIC = "FP8 GMM TFLOP/s (wi+SwiGLU fwd, wo fwd, dLHS) and % of GB300 FP8 peak"
 
 
@@ -227,8 +228,8 @@ def oracle_sample(target_s: float = 12.0, seed: int = 1):
         fl = R * 2.0 * (HID * 2 * FF + FF * HID + HID * FF + 2 * FF * HID) + 2.0 * Mloc * 128 * 512
         return fl, dt
 
-    fl, dt = run(8)
-    R = int(max(8, min(Mloc, 8 * target_s / max(dt, 1e-3))))
+    fl, dt = run(4)
+    R = int(max(4, min(Mloc, 4 * target_s / max(dt, 1e-3))))
     fl, dt = run(R)
     desc = (f"{R} sampled rows of each GMM of the step (wi fwd+SwiGLU, wo fwd, wo and wi dLHS; "
             f"one expert's weights) + a 128x512 block of one expert's wo weight gradient over "
@@ -244,7 +245,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the BF16 comparison and standalone dequant timings")
+    ap.add_argument("--experts", type=int, default=32,
+                    help="local experts (1024 rows each); fewer shrinks the case for profiling")
     args = ap.parse_args()
+    global E, M
+    if args.experts != E:
+        E = args.experts
+        M = E * ROWS_PER_EXPERT
     world, rank, local = dist_setup(args)
     T = M
     flops = step_flops(T)
@@ -323,7 +332,7 @@ def main():
 
     # ----------------------------------------------- extra: BF16 arm, dequant
     extra = {}
-    if rank == 0:
+    if rank == 0 and not args.no_extra:
         w_bf = fb.dequantize_fp8_codes(inp["wi_c"], inp["wi_s"])
         wo_bf = fb.dequantize_fp8_codes(inp["wo_c"], inp["wo_s"])
         torch.cuda.synchronize()
@@ -398,7 +407,8 @@ def main():
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; random FP8 weights of the DeepSeek-V3 MoE shapes)",
-            "config": {"workload": "deepseek_v3_moe_balanced", "E": E, "K": HID,
+            "config": {"workload": "deepseek_v3_moe_balanced" if E == 32 else f"balanced_E{E}",
+                       "E": E, "K": HID,
                        "moe_intermediate": FF, "M": M, "routing": "balanced 1024 rows/expert",
                        "step": "wi fwd+SwiGLU, wo fwd, wo dLHS, wi dLHS, wo dW (tgmm)",
                        "l2": "inputs larger than L2 (~5 GB streamed per step), no flush",

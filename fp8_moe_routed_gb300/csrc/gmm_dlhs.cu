@@ -12,14 +12,18 @@
 //
 // GB300 design (one CTA per SM, persistent), per 128-row x 256-column output
 // tile and 64-wide contraction step:
-//   warp 0       TMA: dout tile [128 x 64] bf16 (K-major, 128-byte swizzle) and
-//                the codes tile [256 x 64] u8 (no swizzle) into a 4-deep ring.
+//   warp 0       TMA: dout tiles [128 x 64] bf16 (K-major, 128-byte swizzle) and
+//                the codes tile [256 x 64] u8 (no swizzle) into a 3-deep ring.
+//                Streaming units cover two m tiles of one expert, so every
+//                dequantized weight tile feeds two accumulators (half the
+//                dequantization per FLOP).
 //   warps 6..13  dequant: e4m3 -> f32, x scale (one f32 multiply), round to
 //                bf16, write the [256 x 64] bf16 B operand in the K-major
 //                128-byte-swizzle layout the tensor core reads (2-deep ring).
 //   warp 1       tcgen05.mma kind::f16 (M=128, N=256, K=16) into TMEM.
-//   warps 2..5   epilogue: TMEM -> bf16 -> row-masked stores; TMEM holds two
-//                accumulators so the epilogue overlaps the next tile.
+//   warps 2..5   epilogue: TMEM -> bf16 -> row-masked stores. TMEM holds two
+//                accumulators: the two m tiles of a streaming unit, or (cached)
+//                consecutive m tiles so that the epilogue overlaps the MMAs.
 // Cached variant (the contraction fits in <= 4 steps, i.e. N <= 256): a work
 // unit is (expert, k tile, run of m tiles); the whole dequantized
 // [256 x N] block stays in shared memory and only dout tiles stream. Both
@@ -40,7 +44,8 @@ namespace dlhs {
 constexpr int kBM = 128;
 constexpr int kBN = 256;                 // output columns (k) per tile = MMA N
 constexpr int kBK = 64;                  // contraction (n) per step
-constexpr int kLdStages = 4;
+constexpr int kLdStages = 4;            // ring slots (cached: A tiles)
+constexpr int kLdStagesStream = 3;      // streaming: 3 slots of [A0 | A1 | C]
 constexpr int kBStages = 2;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB dout tile
 constexpr int kCBytes = kBN * kBK;       // 16 KB codes tile
@@ -51,9 +56,10 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxCachedSteps = 4;       // cached variant: N <= 256
 constexpr int kCachedRun = 8;            // m tiles per cached work unit
 
-// Streaming layout: ld ring (A + C) 4 x 32 KB, B ring 2 x 32 KB = 192 KB.
+// Streaming layout: ld ring [A0 | A1 | C] 3 x 48 KB, B ring 2 x 32 KB = 208 KB.
 // Cached layout: B cache 4 x 32 KB, A ring 4 x 16 KB, C staging 16 KB = 208 KB.
-constexpr size_t kTileBytesStream = (size_t)kLdStages * (kABytes + kCBytes) + kBStages * kBBytes;
+constexpr int kStreamStage = 2 * kABytes + kCBytes;
+constexpr size_t kTileBytesStream = (size_t)kLdStagesStream * kStreamStage + kBStages * kBBytes;
 constexpr size_t kTileBytesCached = (size_t)kMaxCachedSteps * kBBytes + kLdStages * kABytes + kCBytes;
 
 struct Smem {
@@ -84,20 +90,26 @@ struct Unit {
   int e, row0, rows_total, mtiles, j;   // mtiles: m tiles in this unit (streaming: 1)
 };
 
-// Streaming: (e, j, i) with i fastest, 1 m tile per unit.
+// Streaming: (e, j, pair of m tiles), pairs fastest.
 // Cached:    (e, j, run) with runs of up to kCachedRun m tiles.
+template <bool CACHED>
+__device__ __forceinline__ int unit_run(int mt) {
+  return CACHED ? kCachedRun : 2;
+}
+
 template <bool CACHED>
 __device__ __forceinline__ Unit decode_unit(const Smem& s, int E, int nt, int u) {
   Unit r;
   r.e = find_bucket(s.prefix, E, u);
   const int mt = (s.end[r.e] - s.begin[r.e] + kBM - 1) / kBM;
-  const int nruns = CACHED ? (mt + kCachedRun - 1) / kCachedRun : mt;
+  const int run = unit_run<CACHED>(mt);
+  const int nruns = (mt + run - 1) / run;
   const int local = u - s.prefix[r.e];
   r.j = local / nruns;
   const int i = local - r.j * nruns;
-  const int first_tile = CACHED ? i * kCachedRun : i;
+  const int first_tile = i * run;
   r.row0 = s.begin[r.e] + first_tile * kBM;
-  r.mtiles = CACHED ? min(kCachedRun, mt - first_tile) : 1;
+  r.mtiles = min(run, mt - first_tile);
   r.rows_total = s.end[r.e] - r.row0;
   return r;
 }
@@ -186,13 +198,16 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   Smem& s = *reinterpret_cast<Smem*>(tiles + (CACHED ? kTileBytesCached : kTileBytesStream));
-  // Streaming: [ld stage i: A (16 KB) | C (16 KB)] x 4, then B x 2.
+  // Streaming: [ld slot i: A0 (16 KB) | A1 (16 KB) | C (16 KB)] x 3, then B x 2.
   // Cached:    B cache x 4, A x 4, C staging x 1.
+  constexpr int kSlots = CACHED ? kLdStages : kLdStagesStream;
   uint8_t* const ringA = tiles + (CACHED ? kMaxCachedSteps * kBBytes : 0);
-  uint8_t* const ringB = tiles + (CACHED ? 0 : kLdStages * (kABytes + kCBytes));
+  uint8_t* const ringB = tiles + (CACHED ? 0 : kLdStagesStream * kStreamStage);
   uint8_t* const stageC = tiles + kMaxCachedSteps * kBBytes + kLdStages * kABytes;   // cached only
-  auto a_tile = [&](int i) -> uint8_t* { return CACHED ? ringA + i * kABytes : tiles + i * (kABytes + kCBytes); };
-  auto c_tile = [&](int i) -> uint8_t* { return CACHED ? stageC : tiles + i * (kABytes + kCBytes) + kABytes; };
+  auto a_tile = [&](int i, int mi) -> uint8_t* {
+    return CACHED ? ringA + i * kABytes : tiles + i * kStreamStage + mi * kABytes;
+  };
+  auto c_tile = [&](int i) -> uint8_t* { return CACHED ? stageC : tiles + i * kStreamStage + 2 * kABytes; };
   auto b_tile = [&](int i) -> uint8_t* { return ringB + i * kBBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -208,7 +223,8 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int32_t n = 0;
       if (e < E) {
         int mt = (s.end[e] - s.begin[e] + kBM - 1) / kBM;
-        n = (CACHED ? (mt + kCachedRun - 1) / kCachedRun : mt) * nt;
+        const int run = CACHED ? kCachedRun : 2;
+        n = ((mt + run - 1) / run) * nt;
       }
       int32_t incl = n;
 #pragma unroll
@@ -274,28 +290,34 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             ++c_issued;
           }
         }
-        for (int mi = 0; mi < t.mtiles && ok; ++mi) {
-          const int row0 = t.row0 + mi * kBM;
+        if (CACHED) {
+          for (int mi = 0; mi < t.mtiles && ok; ++mi) {
+            const int row0 = t.row0 + mi * kBM;
+            for (int kb = 0; kb < nkb; ++kb) {
+              if (!mbar_wait(&s.ld_empty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
+              mbar_arrive_expect_tx(&s.ld_full[st], kABytes);
+              tma_load_2d(a_tile(st, 0), &tmA, &s.ld_full[st], kb * kBK, row0);
+              ++issued;
+              if (++st == kSlots) { st = 0; ph ^= 1; }
+            }
+          }
+        } else {
           for (int kb = 0; kb < nkb; ++kb) {
             if (!mbar_wait(&s.ld_empty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
-            if (CACHED) {
-              mbar_arrive_expect_tx(&s.ld_full[st], kABytes);
-              tma_load_2d(a_tile(st), &tmA, &s.ld_full[st], kb * kBK, row0);
-            } else {
-              mbar_arrive_expect_tx(&s.ld_full[st], kABytes + kCBytes);
-              tma_load_2d(a_tile(st), &tmA, &s.ld_full[st], kb * kBK, row0);
-              tma_load_3d(c_tile(st), &tmC, &s.ld_full[st], kb * kBK, k0, t.e);
-            }
+            mbar_arrive_expect_tx(&s.ld_full[st], t.mtiles * kABytes + kCBytes);
+            for (int mi = 0; mi < t.mtiles; ++mi)
+              tma_load_2d(a_tile(st, mi), &tmA, &s.ld_full[st], kb * kBK, t.row0 + mi * kBM);
+            tma_load_3d(c_tile(st), &tmC, &s.ld_full[st], kb * kBK, k0, t.e);
             ++issued;
-            if (++st == kLdStages) { st = 0; ph ^= 1; }
+            if (++st == kSlots) { st = 0; ph ^= 1; }
           }
         }
       }
       // drain outstanding copies before the CTA may exit
-      int64_t n_last = issued < kLdStages ? issued : kLdStages;
+      int64_t n_last = issued < kSlots ? issued : kSlots;
       for (int64_t i = 1; i <= n_last; ++i) {
         int64_t idx = issued - i;
-        mbar_wait(&s.ld_full[idx % kLdStages], (uint32_t)((idx / kLdStages) & 1), kWhereDrain);
+        mbar_wait(&s.ld_full[idx % kSlots], (uint32_t)((idx / kSlots) & 1), kWhereDrain);
       }
       if (CACHED && c_issued > 0) mbar_wait(&s.c_full, (uint32_t)((c_issued - 1) & 1), kWhereDrain);
     }
@@ -311,47 +333,58 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int acc = 0;
       uint32_t aph = 0;
       bool ok = true;
+      auto issue = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr, int kb) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = make_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = make_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B);
+          mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
+        }
+      };
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit t = decode_unit<CACHED>(s, E, nt, u);
-        for (int mi = 0; mi < t.mtiles && ok; ++mi) {
-          if (!mbar_wait(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(acc * kBN);
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait(&s.ld_full[st], ph, kWhereMma)) { ok = false; break; }
-            int bi;
-            if (CACHED) {
-              bi = kb;
+        if (CACHED) {
+          // one m tile per accumulator, accumulators alternate (epilogue overlaps)
+          for (int mi = 0; mi < t.mtiles && ok; ++mi) {
+            if (!mbar_wait(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * kBN);
+            for (int kb = 0; kb < nkb; ++kb) {
+              if (!mbar_wait(&s.ld_full[st], ph, kWhereMma)) { ok = false; break; }
               // the cache slot kb is (re)filled once per unit
               if (mi == 0 && !mbar_wait(&s.b_full[kb], (uint32_t)(cached_fills & 1), kWhereMma)) { ok = false; break; }
-            } else {
-              bi = bst;
-              if (!mbar_wait(&s.b_full[bst], bph, kWhereMma)) { ok = false; break; }
+              tc_fence_after();
+              issue(d, smem_u32(a_tile(st, 0)), smem_u32(b_tile(kb)), kb);
+              mma_commit(&s.ld_empty[st]);
+              if (mi + 1 == t.mtiles) mma_commit(&s.b_empty[kb]);   // slot refillable by the next unit
+              if (++st == kSlots) { st = 0; ph ^= 1; }
             }
+            if (!ok) break;
+            mma_commit(&s.tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+          }
+          ++cached_fills;
+        } else {
+          // both m tiles of the unit share each dequantized B tile
+          if (!mbar_wait(&s.tempty[0], aph ^ 1, kWhereMma)) { ok = false; break; }
+          tc_fence_after();
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait(&s.ld_full[st], ph, kWhereMma)) { ok = false; break; }
+            if (!mbar_wait(&s.b_full[bst], bph, kWhereMma)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(a_tile(st));
-            const uint32_t b_addr = smem_u32(b_tile(bi));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = make_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bd = make_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B);
-              mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
-            }
+            const uint32_t b_addr = smem_u32(b_tile(bst));
+            for (int mi = 0; mi < t.mtiles; ++mi)
+              issue(tmem + (uint32_t)(mi * kBN), smem_u32(a_tile(st, mi)), b_addr, kb);
             mma_commit(&s.ld_empty[st]);
-            if (!CACHED) {
-              mma_commit(&s.b_empty[bst]);
-              if (++bst == kBStages) { bst = 0; bph ^= 1; }
-            } else if (mi + 1 == t.mtiles) {
-              mma_commit(&s.b_empty[kb]);     // cache slot may be refilled by the next unit
-            }
-            if (++st == kLdStages) { st = 0; ph ^= 1; }
+            mma_commit(&s.b_empty[bst]);
+            if (++bst == kBStages) { bst = 0; bph ^= 1; }
+            if (++st == kSlots) { st = 0; ph ^= 1; }
           }
           if (!ok) break;
-          mma_commit(&s.tfull[acc]);
-          acc ^= 1;
-          if (acc == 0) aph ^= 1;
+          mma_commit(&s.tfull[0]);
+          aph ^= 1;
         }
-        if (CACHED) ++cached_fills;
       }
       mma_commit(&s.drain);
       mbar_wait(&s.drain, 0, kWhereDrain);
@@ -362,23 +395,37 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int r = quarter * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = decode_unit<CACHED>(s, E, nt, u);
-      bool ok = true;
+      if (!CACHED) {
+        if (!mbar_wait_warp(&s.tfull[0], aph, kWhereEpilogue)) { ok = false; break; }
+        tc_fence_after();
+      }
       for (int mi = 0; mi < t.mtiles; ++mi) {
         const int rows = min(kBM, t.rows_total - mi * kBM);
         const bool row_ok = r < rows;
         const int64_t row = (int64_t)t.row0 + mi * kBM + r;
-        if (!mbar_wait(&s.tfull[acc], aph, kWhereEpilogue)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+        int col_acc = mi;
+        if (CACHED) {
+          if (!mbar_wait_warp(&s.tfull[acc], aph, kWhereEpilogue)) { ok = false; break; }
+          tc_fence_after();
+          col_acc = acc;
+        }
+        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(col_acc * kBN);
         store_tile(tbase, r, row_ok, dlhs + row * K, t.j * kBN, K);
-        tc_fence_before();
-        mbar_arrive(&s.tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1;
+        if (CACHED) {
+          tc_fence_before();
+          mbar_arrive(&s.tempty[acc]);
+          acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        }
       }
-      if (!ok) break;
+      if (!CACHED && ok) {
+        tc_fence_before();
+        mbar_arrive(&s.tempty[0]);
+        aph ^= 1;
+      }
     }
   } else {
     // ========================== dequant warps ============================
@@ -423,7 +470,7 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_arrive(&s.b_full[bst]);
             mbar_arrive(&s.ld_empty[st]);
           }
-          if (++st == kLdStages) { st = 0; ph ^= 1; }
+          if (++st == kSlots) { st = 0; ph ^= 1; }
           if (++bst == kBStages) { bst = 0; bph ^= 1; }
         }
       }

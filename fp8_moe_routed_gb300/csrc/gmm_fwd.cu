@@ -272,7 +272,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool row_ok = r < t.rows;
       const int64_t row = (int64_t)t.row0 + r;
       const float sxr = (FP8 && row_ok) ? __ldg(sx + row) : 1.0f;
-      if (!failed && !mbar_wait(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
+      if (!failed && !mbar_wait_warp(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
       if (failed) {
         acc ^= 1;
         if (acc == 0) aph ^= 1;

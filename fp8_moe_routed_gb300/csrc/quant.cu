@@ -4,7 +4,7 @@
 //    row over the whole K, scale = max(amax, 1e-12) / 448, codes = e4m3(x / scale)
 //    ("MoE: native FP8 QAT for routed-expert GMMs", Description and
 //    Implementation: in-kernel full-K activation quantization with an f32 scale).
-//    One warp per row, the row held in registers between the amax pass and the
+//    One CTA per row, the row held in registers between the amax pass and the
 //    cast pass; rows at or past T = sum(group_sizes) are never read.
 //
 //  * tgmm_quantize_tiles_kernel: the weight-gradient operands, per 128-row tile
@@ -56,26 +56,32 @@ __device__ __forceinline__ uint2 quant8(uint4 v, float s) {
 }
 
 // ------------------------------------------------------------------------ a1
-// One warp per row; each lane holds up to MAXC 16-byte chunks of the row.
-template <int MAXC>
-__global__ void __launch_bounds__(256) quantize_rows_kernel(
+// One CTA of 256 threads per row (grid-stride over rows): each thread holds CPT
+// 16-byte chunks of the row in registers, the row amax is reduced across the
+// CTA, then every thread casts its own chunks. Few registers per thread keep
+// many rows in flight per SM, which is what an HBM-bound pass needs.
+constexpr int kQThreads = 256;
+
+template <int CPT>
+__global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
     int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
   __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
   __shared__ int32_t s_T;
+  __shared__ float s_red[2][kQThreads / 32];
   load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
   __syncthreads();
   const int T = s_T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = K >> 3;   // K % 8 == 0
-  const int warps_total = gridDim.x * 8;
-  for (int64_t m = (int64_t)blockIdx.x * 8 + warp; m < T; m += warps_total) {
+  int buf = 0;
+  for (int64_t m = blockIdx.x; m < T; m += gridDim.x) {
     const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
-    uint4 v[MAXC];
+    uint4 v[CPT];
     uint32_t amax2 = 0;
 #pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      int c = lane + 32 * i;
+    for (int i = 0; i < CPT; ++i) {
+      const int c = threadIdx.x + kQThreads * i;
       if (c < nchunk) {
         v[i] = __ldg(row + c);
         amax2 = bf16x2_absmax(amax2, v[i].x);
@@ -87,33 +93,41 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
     float amax = bf16x2_hmax_to_f32(amax2);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if (lane == 0) s_red[buf][warp] = amax;
+    __syncthreads();
+    amax = s_red[buf][0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[buf][w]);
+    buf ^= 1;   // the next row reduces into the other buffer: no second barrier needed
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
 #pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      int c = lane + 32 * i;
+    for (int i = 0; i < CPT; ++i) {
+      const int c = threadIdx.x + kQThreads * i;
       if (c < nchunk) qrow[c] = quant8(v[i], s);
     }
-    if (lane == 0) sx[m] = s;
+    if (threadIdx.x == 0) sx[m] = s;
   }
 }
 
-// Rows longer than the register cache: the cast pass re-reads the row (L2 hit).
-__global__ void __launch_bounds__(256) quantize_rows_stream_kernel(
+// Rows longer than the register cache (K > 8192): the cast pass re-reads the
+// row (L2 hit).
+__global__ void __launch_bounds__(kQThreads) quantize_rows_stream_kernel(
     const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
     int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
   __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
   __shared__ int32_t s_T;
+  __shared__ float s_red[2][kQThreads / 32];
   load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
   __syncthreads();
   const int T = s_T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = K >> 3;
-  const int warps_total = gridDim.x * 8;
-  for (int64_t m = (int64_t)blockIdx.x * 8 + warp; m < T; m += warps_total) {
+  int buf = 0;
+  for (int64_t m = blockIdx.x; m < T; m += gridDim.x) {
     const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
     uint32_t amax2 = 0;
-    for (int c = lane; c < nchunk; c += 32) {
+    for (int c = threadIdx.x; c < nchunk; c += kQThreads) {
       uint4 v = __ldg(row + c);
       amax2 = bf16x2_absmax(amax2, v.x);
       amax2 = bf16x2_absmax(amax2, v.y);
@@ -123,10 +137,16 @@ __global__ void __launch_bounds__(256) quantize_rows_stream_kernel(
     float amax = bf16x2_hmax_to_f32(amax2);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if (lane == 0) s_red[buf][warp] = amax;
+    __syncthreads();
+    amax = s_red[buf][0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[buf][w]);
+    buf ^= 1;
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
-    for (int c = lane; c < nchunk; c += 32) qrow[c] = quant8(__ldg(row + c), s);
-    if (lane == 0) sx[m] = s;
+    for (int c = threadIdx.x; c < nchunk; c += kQThreads) qrow[c] = quant8(__ldg(row + c), s);
+    if (threadIdx.x == 0) sx[m] = s;
   }
 }
 
@@ -234,19 +254,20 @@ cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const
                                         int E, uint8_t* q, float* sx, int num_sms, int report,
                                         cudaStream_t s) {
   using namespace fp8moe;
-  int64_t blocks_needed = (M + 7) / 8;
-  int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
+  // Up to 8 row-CTAs resident per SM; the grid strides over the rows.
+  int64_t cap = (int64_t)num_sms * 8;
+  int grid = (int)(M < cap ? M : cap);
   if (grid < 1) grid = 1;
   const auto* x = static_cast<const __nv_bfloat16*>(lhs);
-  const int nchunk_lane = (K / 8 + 31) / 32;
-  if (nchunk_lane <= 8)
-    quantize_rows_kernel<8><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
-  else if (nchunk_lane <= 16)
-    quantize_rows_kernel<16><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
-  else if (nchunk_lane <= 32)
-    quantize_rows_kernel<32><<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  const int cpt = (K / 8 + kQThreads - 1) / kQThreads;
+  if (cpt <= 1)
+    quantize_rows_kernel<1><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  else if (cpt <= 2)
+    quantize_rows_kernel<2><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+  else if (cpt <= 4)
+    quantize_rows_kernel<4><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
   else
-    quantize_rows_stream_kernel<<<grid, 256, 0, s>>>(x, M, K, gs, E, q, sx, report);
+    quantize_rows_stream_kernel<<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,9 @@
 // 256-wide n tile); n tiles of one k tile are adjacent so the A slots are
 // shared through L2.
 //   warp 0      TMA: qx slot [128 rows x 128 k] and qd slot [128 rows x 128 n],
-//               both row-major = MN-major operands, 128-byte swizzle.
+//               both row-major = MN-major operands, 128-byte swizzle; and the
+//               segment's 128 + 128 channel scales by bulk copy into a scale
+//               ring that the rescale warps release.
 //   warp 1      tcgen05.mma kind::f8f6f4, M=128 (k), N=128 (n), K=32 rows, four
 //               per segment, into one of two TMEM partial buffers.
 //   warps 2..9  rescale: each thread owns one k row and 64 n columns of the
@@ -48,17 +50,20 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;    // 320
 constexpr int kTmemCols = 512;
 constexpr int kXpose = 32 * 32 * 4;               // per-warp transpose buffer
+constexpr int kSRing = 4;                         // scale ring slots
 
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t sfull[kSRing];
+  uint64_t sempty[kSRing];
   uint64_t drain;
   uint32_t tmem_base;
   int32_t T;
   int32_t total_units;
-  alignas(16) float sd[2][kBN];
+  alignas(16) float sring[kSRing][2][128];   // [slot][0: sx over k, 1: sd over n]
   int32_t begin[kMaxExperts];
   int32_t end[kMaxExperts];
   int32_t segbase[kMaxExperts + 1];
@@ -66,10 +71,6 @@ struct Smem {
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kEpiWarps * kXpose + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
@@ -117,6 +118,10 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         mbar_init(&s.tfull[i], 1);
         mbar_init(&s.tempty[i], kEpiWarps * 32);
       }
+      for (int i = 0; i < kSRing; ++i) {
+        mbar_init(&s.sfull[i], 1);
+        mbar_init(&s.sempty[i], kEpiWarps * 32);
+      }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
     }
@@ -140,12 +145,24 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         const int e = u / units_per_e, rem = u - e * units_per_e;
         const int kt = rem / nnt, ntile = rem - kt * nnt;
         const int q0 = s.segbase[e], q1 = s.segbase[e + 1];
+        // K, N % 16 == 0: the valid part of a 128-wide scale row is a multiple
+        // of 64 bytes, so both bulk copies keep 16-byte alignment and size.
+        const uint32_t kbytes = (uint32_t)min(kBK, K - kt * kBK) * 4u;
+        const uint32_t nbytes = (uint32_t)min(kBN, N - ntile * kBN) * 4u;
         for (int q = q0; q < q1; ++q) {
           if (!mbar_wait(&s.empty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
+          const int ss = (int)(issued % kSRing);
+          if (!mbar_wait(&s.sempty[ss], (uint32_t)(((issued / kSRing) & 1) ^ 1), kWhereProducer)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&s.full[st], kStageBytes);
           uint8_t* a = tiles + st * kStageBytes;
           tma_load_2d(a, &tmX, &s.full[st], kt * kBK, q * 128);
           tma_load_2d(a + kXBytes, &tmD, &s.full[st], ntile * kBN, q * 128);
+          mbar_arrive_expect_tx(&s.sfull[ss], kbytes + nbytes);
+          bulk_load(s.sring[ss][0], sx + (int64_t)q * K + kt * kBK, kbytes, &s.sfull[ss]);
+          bulk_load(s.sring[ss][1], sd + (int64_t)q * N + ntile * kBN, nbytes, &s.sfull[ss]);
           ++issued;
           if (++st == kStages) { st = 0; ph ^= 1; }
         }
@@ -154,6 +171,11 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
       for (int64_t i = 1; i <= n_last; ++i) {
         int64_t idx = issued - i;
         mbar_wait(&s.full[idx % kStages], (uint32_t)((idx / kStages) & 1), kWhereDrain);
+      }
+      n_last = issued < kSRing ? issued : kSRing;
+      for (int64_t i = 1; i <= n_last; ++i) {
+        int64_t idx = issued - i;
+        mbar_wait(&s.sfull[idx % kSRing], (uint32_t)((idx / kSRing) & 1), kWhereDrain);
       }
     }
   } else if (warp == 1) {
@@ -197,40 +219,30 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     const int ew = warp - 2;                 // 0..7
     const int quarter = warp & 3;            // TMEM lanes 32*quarter ..
     const int half = ew >> 2;                // columns [64*half, 64*half + 64)
-    const int et = threadIdx.x - 64;         // 0..255
     const int r = quarter * 32 + lane;       // k row inside the tile
     float* xp = xpose + ew * (kXpose / 4);
     int acc = 0;
     uint32_t aph = 0;
-    int sb = 0;
-    // A timed-out wait marks the thread failed; it keeps iterating (skipping TMEM
-    // and stores) so that every thread passes the same named barriers.
+    int64_t used = 0;                        // scale ring position
     bool failed = false;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    for (int u = blockIdx.x; u < total && !failed; u += gridDim.x) {
       const int e = u / units_per_e, rem = u - e * units_per_e;
       const int kt = rem / nnt, ntile = rem - kt * nnt;
       const int q0 = s.segbase[e], q1 = s.segbase[e + 1];
-      const int k = kt * kBK + r;
       float a[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) a[i] = 0.0f;
       for (int q = q0; q < q1; ++q) {
-        if (et < kBN) {
-          const int n = ntile * kBN + et;
-          s.sd[sb][et] = n < N ? __ldg(sd + (int64_t)q * N + n) : 0.0f;
-        }
-        named_bar_sync(1, kEpiWarps * 32);
-        const float sxk = k < K ? __ldg(sx + (int64_t)q * K + k) : 0.0f;
-        if (!failed && !mbar_wait(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
-        if (failed) {
-          acc ^= 1;
-          if (acc == 0) aph ^= 1;
-          sb ^= 1;
-          continue;
+        const int ss = (int)(used % kSRing);
+        if (!mbar_wait_warp(&s.sfull[ss], (uint32_t)((used / kSRing) & 1), kWhereEpilogue) ||
+            !mbar_wait_warp(&s.tfull[acc], aph, kWhereEpilogue)) {
+          failed = true;
+          break;
         }
         tc_fence_after();
+        const float sxk = s.sring[ss][0][r];
+        const float4* sdv = reinterpret_cast<const float4*>(&s.sring[ss][1][half * 64]);
         const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + half * 64);
-        const float4* sdv = reinterpret_cast<const float4*>(&s.sd[sb][half * 64]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
@@ -247,11 +259,12 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         }
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
+        mbar_arrive(&s.sempty[ss]);
+        ++used;
         acc ^= 1;
         if (acc == 0) aph ^= 1;
-        sb ^= 1;
       }
-      if (failed) continue;
+      if (failed) break;
       // store: 2 chunks of [32 k rows x 32 n] through the per-warp transpose
       // buffer (16-byte chunk c4 of row i stored at chunk c4 ^ (i & 7)).
       const int k_warp0 = kt * kBK + quarter * 32;
