@@ -38,7 +38,7 @@ EXPORTS = [
     "fp8moe_gmm_dlhs_fp8", "fp8moe_gmm_dlhs_fp8_path", "fp8moe_tgmm_drhs_quant",
     "fp8moe_dequantize_fp8_codes", "fp8moe_gmm_bf16_fwd", "fp8moe_quantize_rows",
     "fp8moe_tgmm_quantize_tiles", "fp8moe_read_status", "fp8moe_status_string",
-    "fp8moe_last_cuda_error", "fp8moe_num_sms",
+    "fp8moe_last_cuda_error", "fp8moe_num_sms", "fp8moe_gmm_silu_fp8_fwd_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -81,6 +81,7 @@ def load(build_if_missing: bool = True):
             "fp8moe_status_string": ([I32], ctypes.c_char_p),
             "fp8moe_last_cuda_error": ([], I32),
             "fp8moe_num_sms": ([], I32),
+            "fp8moe_gmm_silu_fp8_fwd_noalloc": ([P, I64, I64, P, P, I32, I64, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -167,6 +168,27 @@ def gmm_fp8_fwd(lhs, codes, scale, group_sizes, out=None, workspace=None):
 def gmm_silu_fp8_fwd(lhs, codes, scale, group_sizes, out=None, workspace=None):
     """wi forward with fused SwiGLU: bf16 [M, N/2] (see fp8moe_gmm_silu_fp8_fwd)."""
     return _fwd(lhs, codes, scale, group_sizes, out, workspace, silu=True)
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def gmm_silu_fp8_fwd_noalloc(lhs, codes, scale, group_sizes, out):
+    """wi forward without a caller workspace: the library's fixed 32 MiB device
+    array stands in for it (see fp8moe_gmm_silu_fp8_fwd_noalloc). ``out`` must be
+    given; this call allocates nothing."""
+    L = load()
+    _req(lhs, torch.bfloat16, "lhs", 2)
+    _req(codes, torch.uint8, "codes", 3)
+    _req(scale, torch.float32, "scale", 2)
+    _req(group_sizes, torch.int32, "group_sizes", 1)
+    _req(out, torch.bfloat16, "out", 2)
+    M, K = lhs.shape
+    E, _, N = codes.shape
+    _check(L.fp8moe_gmm_silu_fp8_fwd_noalloc(_ptr(lhs), M, K, _ptr(codes), _ptr(scale), E, N,
+                                             _ptr(group_sizes), _ptr(out), _stream(lhs.device)),
+           "fp8moe_gmm_silu_fp8_fwd_noalloc")
+    return out
 
 
 def gmm_dlhs_fp8(dout, codes, scale, group_sizes, out=None, path: Optional[int] = None):

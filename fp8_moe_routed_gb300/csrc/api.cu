@@ -464,6 +464,8 @@ const char* fp8moe_status_string(int code) {
 
 int fp8moe_last_cuda_error(void) { return t_last_cuda_error; }
 
+void fp8moe_internal_set_cuda_error(int e) { t_last_cuda_error = e; }
+
 int fp8moe_num_sms(void) {
   int sms = 0;
   if (device_init(&sms) != FP8MOE_OK) return 0;

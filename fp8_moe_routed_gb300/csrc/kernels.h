@@ -54,6 +54,9 @@ struct TgmmArgs {
 };
 cudaError_t fp8moe_launch_tgmm(const TgmmArgs& a, int num_sms, cudaStream_t s);
 
+// Records the CUDA error that fp8moe_last_cuda_error() reports (api.cu).
+extern "C" void fp8moe_internal_set_cuda_error(int e);
+
 uint32_t fp8moe_status_take_quant(cudaStream_t s);
 uint32_t fp8moe_status_take_dequant(cudaStream_t s);
 uint32_t fp8moe_status_take_gmm_fwd(cudaStream_t s);

@@ -165,6 +165,24 @@ int fp8moe_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int
  * since the last call, and clears them. */
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags);
 
+/* The wi forward of fp8moe_gmm_silu_fp8_fwd for callers that cannot allocate
+ * device memory (a plugin inside a framework whose caching allocator holds
+ * nearly all of it, or a runtime that forbids allocations after start-up).  The
+ * pages have no counterpart: it is an interface variant, not a step of the
+ * method.  Arguments and results are those of fp8moe_gmm_silu_fp8_fwd minus the
+ * workspace, which comes from a fixed 32 MiB device array that the library holds
+ * on every GPU it is loaded on until the process exits; sizes whose workspace
+ * (fp8moe_workspace_size(FP8MOE_OP_GMM_SILU_FP8_FWD, ...)) exceeds it return
+ * FP8MOE_EWORKSPACE and launch nothing.  The first call on a device looks up the
+ * array's device address (make that call before any stream capture).  All calls
+ * share the array, so calls that overlap on the GPU race; each call rewrites
+ * everything it reads, so nothing needs clearing between calls.  Allocates
+ * nothing. */
+int fp8moe_gmm_silu_fp8_fwd_noalloc(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
+                                    const float* scale, int32_t E, int64_t N,
+                                    const int32_t* group_sizes, void* out,
+                                    fp8moe_stream_t stream);
+
 /* Text for a return code. */
 const char* fp8moe_status_string(int code);
 
