@@ -237,7 +237,39 @@ def oracle_sample(target_s: float = 12.0, seed: int = 1):
     return fl / dt / 1e12, orc.num_threads(), desc
 
 
+def summarize_launches(path: str) -> str:
+    """Markdown table (kernel, launches, total/mean device time, share) from an
+    ncu launch list taken with --metrics gpu__time_duration.sum --csv."""
+    import collections
+    import csv
+    rows = list(csv.reader(open(path)))
+    hdr, data = None, []
+    for r in rows:
+        if r and r[0] == "ID":
+            hdr = r
+            continue
+        if hdr and len(r) == len(hdr):
+            data.append(dict(zip(hdr, r)))
+    agg = collections.OrderedDict()
+    for d in data:
+        if d["Metric Name"] != "gpu__time_duration.sum":
+            continue
+        name = d["Kernel Name"].split("(")[0]
+        v = float(d["Metric Value"].replace(",", ""))
+        unit = d["Metric Unit"]
+        us = v * 1e3 if unit in ("ms", "msecond") else v / 1e3 if unit in ("ns", "nsecond") else v
+        agg.setdefault(name, []).append(us)
+    tot = sum(sum(v) for v in agg.values()) or 1.0
+    out = ["| kernel | launches | total us | mean us | share |", "|---|---|---|---|---|"]
+    for k, v in sorted(agg.items(), key=lambda kv: -sum(kv[1])):
+        out.append(f"| `{k}` | {len(v)} | {sum(v):.1f} | {sum(v) / len(v):.1f} | {sum(v) / tot:.3f} |")
+    return "\n".join(out)
+
+
 def main():
+    if len(sys.argv) == 3 and sys.argv[1] == "--summarize-launches":
+        print(summarize_launches(sys.argv[2]))
+        return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
