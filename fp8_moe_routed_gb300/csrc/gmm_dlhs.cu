@@ -256,7 +256,7 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(&s.c_empty, kDqWarps);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 128);
+        mbar_init(&s.tempty[i], 4);   // one elected lane per epilogue warp
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -416,14 +416,16 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         store_tile(tbase, r, row_ok, dlhs + row * K, t.j * kBN, K);
         if (CACHED) {
           tc_fence_before();
-          mbar_arrive(&s.tempty[acc]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.tempty[acc]);
           acc ^= 1;
           if (acc == 0) aph ^= 1;
         }
       }
       if (!CACHED && ok) {
         tc_fence_before();
-        mbar_arrive(&s.tempty[0]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[0]);
         aph ^= 1;
       }
     }

@@ -138,7 +138,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 128);
+        mbar_init(&s.tempty[i], 4);   // one elected lane per epilogue warp
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -338,7 +338,8 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       tc_fence_before();
-      mbar_arrive(&s.tempty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);
       acc ^= 1;
       if (acc == 0) aph ^= 1;
       sb ^= 1;

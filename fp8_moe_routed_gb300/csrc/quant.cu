@@ -13,9 +13,11 @@
 //    per (tile, group) segment, rows outside the segment zeroed, so the
 //    contraction kernel can TMA whole slots without masking.
 //
-// Both divide with IEEE round-to-nearest (this file is compiled without fast
-// math) and cast with cvt.rn.satfinite, so codes and scales are bit-exact with a
-// plain f32 reading of the definition.
+// Both produce exactly the codes of RN_e4m3(RN_f32(x / scale)) (see
+// e4m3_quotient: a reciprocal multiply, with the IEEE division taken wherever
+// the two could round differently) and cast with cvt.rn.satfinite, so codes and
+// scales are bit-exact with a plain f32 reading of the definition. The scale
+// itself is always an IEEE division.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -39,15 +41,35 @@ __device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t v) {
   return fmaxf(bf16lo_to_f32(v), bf16hi_to_f32(v));
 }
 
+// A value whose e4m3 rounding equals that of the correctly rounded f32 quotient
+// RN(x / s). r = RN(1 / s).
+//   y = RN(x * r) = (x / s)(1 + d), |d| <= 2^-23 + 2^-48, so y is within 3 f32
+//   ulps of RN(x / s). Rounding to e4m3 can only differ between the two when a
+//   rounding boundary lies between them. In the normal e4m3 range the
+//   boundaries are the midpoints between 4-significant-bit values: f32 numbers
+//   whose low 20 mantissa bits are exactly 0x80000. Grid points themselves and
+//   powers of two are not boundaries, and everything past 448 saturates. So y is
+//   returned unless its low 20 bits are within 4 of 0x80000 or |y| < 2^-6 (the
+//   e4m3 subnormal range, where the boundaries sit elsewhere); then the exact
+//   IEEE quotient is computed. Infinite and NaN inputs take the fast path and
+//   convert exactly as the quotient would (saturate, NaN).
+__device__ __forceinline__ float e4m3_quotient(float x, float s, float r) {
+  float y = __fmul_rn(x, r);
+  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
+  const bool near_mid = ((b & 0xFFFFFu) - 0x7FFFCu) < 9u;
+  if (near_mid || b < 0x3C800000u) y = __fdiv_rn(x, s);
+  return y;
+}
+
 // 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2).
-__device__ __forceinline__ uint2 quant8(uint4 v, float s) {
+__device__ __forceinline__ uint2 quant8(uint4 v, float s, float r) {
   uint2 o;
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint16_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float lo = __fdiv_rn(bf16lo_to_f32(w[i]), s);
-    float hi = __fdiv_rn(bf16hi_to_f32(w[i]), s);
+    float lo = e4m3_quotient(bf16lo_to_f32(w[i]), s, r);
+    float hi = e4m3_quotient(bf16hi_to_f32(w[i]), s, r);
     c[i] = f32x2_to_e4m3x2(lo, hi);
   }
   o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
@@ -75,15 +97,36 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = K >> 3;   // K % 8 == 0
   int buf = 0;
+  // The next row's loads are issued before this row's cast, so the HBM latency
+  // of one row overlaps the arithmetic of the previous one.
+  uint4 nxt[CPT];
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) nxt[i] = make_uint4(0u, 0u, 0u, 0u);
+  if ((int64_t)blockIdx.x < T) {
+    const uint4* row = reinterpret_cast<const uint4*>(lhs + (int64_t)blockIdx.x * K);
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = threadIdx.x + kQThreads * i;
+      if (c < nchunk) nxt[i] = __ldg(row + c);
+    }
+  }
   for (int64_t m = blockIdx.x; m < T; m += gridDim.x) {
-    const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
     uint4 v[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) v[i] = nxt[i];
+    if (m + gridDim.x < T) {
+      const uint4* row = reinterpret_cast<const uint4*>(lhs + (m + gridDim.x) * K);
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = threadIdx.x + kQThreads * i;
+        if (c < nchunk) nxt[i] = __ldg(row + c);
+      }
+    }
     uint32_t amax2 = 0;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = threadIdx.x + kQThreads * i;
       if (c < nchunk) {
-        v[i] = __ldg(row + c);
         amax2 = bf16x2_absmax(amax2, v[i].x);
         amax2 = bf16x2_absmax(amax2, v[i].y);
         amax2 = bf16x2_absmax(amax2, v[i].z);
@@ -100,11 +143,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[buf][w]);
     buf ^= 1;   // the next row reduces into the other buffer: no second barrier needed
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
+    const float rs = __frcp_rn(s);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = threadIdx.x + kQThreads * i;
-      if (c < nchunk) qrow[c] = quant8(v[i], s);
+      if (c < nchunk) qrow[c] = quant8(v[i], s, rs);
     }
     if (threadIdx.x == 0) sx[m] = s;
   }
@@ -145,7 +189,8 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_stream_kernel(
     buf ^= 1;
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
-    for (int c = threadIdx.x; c < nchunk; c += kQThreads) qrow[c] = quant8(__ldg(row + c), s);
+    const float rs = __frcp_rn(s);
+    for (int c = threadIdx.x; c < nchunk; c += kQThreads) qrow[c] = quant8(__ldg(row + c), s, rs);
     if (threadIdx.x == 0) sx[m] = s;
   }
 }
@@ -174,15 +219,24 @@ __device__ __forceinline__ void build_segments_warp0(const int32_t* s_begin, con
   if (lane == 0) s_segbase[E] = carry;
 }
 
-// Work unit = (segment, 2048-column chunk) over the columns of lhs then dout.
-// Each warp owns 256 columns (8 per lane).
-__global__ void __launch_bounds__(256) tgmm_quantize_tiles_kernel(
+// Work unit = (segment, 128-column chunk) over the columns of lhs then dout.
+// The segment's rows of the chunk are staged once in shared memory (one HBM
+// read), the per-column amax comes from there, then every thread casts its own
+// 16-byte pieces into the zero-padded slot.
+constexpr int kTQThreads = 256;
+constexpr int kTQCols = 128;
+constexpr int kTQRowBytes = kTQCols * 2;   // 256 B of bf16 per staged row
+
+__global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
     const __nv_bfloat16* __restrict__ lhs, const __nv_bfloat16* __restrict__ dout, int64_t M,
     int K, int N, const int32_t* __restrict__ gs, int E, int64_t Smax,
     uint8_t* __restrict__ qx, float* __restrict__ sx, uint8_t* __restrict__ qd,
     float* __restrict__ sd, int report) {
   __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts], s_segbase[kMaxExperts + 1];
   __shared__ int32_t s_T;
+  __shared__ __align__(16) uint8_t s_tile[128 * kTQRowBytes];   // [row][128 bf16]
+  __shared__ uint32_t s_part[4][kTQCols / 2];                   // bf16x2 partial amax
+  __shared__ float s_scale[kTQCols];
   load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
   __syncthreads();
   build_segments_warp0(s_begin, s_end, E, s_segbase);
@@ -192,56 +246,91 @@ __global__ void __launch_bounds__(256) tgmm_quantize_tiles_kernel(
     if (blockIdx.x == 0 && threadIdx.x == 0) status_set(kStatusTooManySegments);
     return;
   }
-  const int ck = (K + 2047) / 2048, cn = (N + 2047) / 2048, cpq = ck + cn;
+  const int ck = (K + kTQCols - 1) / kTQCols, cn = (N + kTQCols - 1) / kTQCols, cpq = ck + cn;
   const int64_t units = (int64_t)S * cpq;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+  const int piece = tid & 15;         // 16-byte piece (8 columns) of a staged row
+  const int prow = tid >> 4;          // first row of this thread, step 16
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int qi = (int)(u / cpq), ch = (int)(u % cpq);
     const int e = find_bucket(s_segbase, E, qi);
     const int t = s_begin[e] / 128 + (qi - s_segbase[e]);
     const int r0 = max(s_begin[e], t * 128), r1 = min(s_end[e], t * 128 + 128);
+    const int lo = r0 - t * 128, hi = r1 - t * 128;            // slot rows of the segment
     const bool is_x = ch < ck;
     const int C = is_x ? K : N;
-    const int c0 = (is_x ? ch : ch - ck) * 2048 + warp * 256 + lane * 8;
-    if (c0 >= C) continue;
+    const int c0 = (is_x ? ch : ch - ck) * kTQCols;
+    const int ncols = min(kTQCols, C - c0);                     // multiple of 16
     const __nv_bfloat16* src = is_x ? lhs : dout;
     uint8_t* qo = (is_x ? qx : qd) + (int64_t)qi * 128 * C;
     float* so = (is_x ? sx : sd) + (int64_t)qi * C;
-    // pass 1: per-column absmax over the segment rows
-    uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-    for (int m = r0; m < r1; ++m) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)m * C + c0));
-      a0 = bf16x2_absmax(a0, v.x);
-      a1 = bf16x2_absmax(a1, v.y);
-      a2 = bf16x2_absmax(a2, v.z);
-      a3 = bf16x2_absmax(a3, v.w);
-    }
-    float s[8];
-    const uint32_t aw[4] = {a0, a1, a2, a3};
+    const bool pin = piece * 8 < ncols;
+    // stage: rows [lo, hi) of the slot, 16 threads per 256-byte row
+    uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      s[2 * i] = __fdiv_rn(fmaxf(bf16lo_to_f32(aw[i]), kEps), kE4m3Max);
-      s[2 * i + 1] = __fdiv_rn(fmaxf(bf16hi_to_f32(aw[i]), kEps), kE4m3Max);
+    for (int i = 0; i < 8; ++i) {
+      const int rr = prow + 16 * i;
+      if (pin && rr >= lo && rr < hi)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(t * 128 + rr) * C + c0) + piece);
     }
-    reinterpret_cast<float4*>(so + c0)[0] = make_float4(s[0], s[1], s[2], s[3]);
-    reinterpret_cast<float4*>(so + c0)[1] = make_float4(s[4], s[5], s[6], s[7]);
-    // pass 2: codes into the slot; slot rows outside the segment are zero
-    for (int r = 0; r < 128; ++r) {
-      const int m = t * 128 + r;
-      uint2 o = make_uint2(0u, 0u);
-      if (m >= r0 && m < r1) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)m * C + c0));
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint16_t c[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          c[i] = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_to_f32(w[i]), s[2 * i]),
-                                 __fdiv_rn(bf16hi_to_f32(w[i]), s[2 * i + 1]));
-        o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
-        o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+    for (int i = 0; i < 8; ++i) {
+      const int rr = prow + 16 * i;
+      if (pin && rr >= lo && rr < hi)
+        *reinterpret_cast<uint4*>(s_tile + rr * kTQRowBytes + piece * 16) = v[i];
+    }
+    __syncthreads();
+    // column amax: thread -> column pair cp, rows of quarter rq
+    {
+      const int cp = tid & 63, rq = tid >> 6;
+      uint32_t m2 = 0;
+      const int a = max(lo, rq * 32), b = min(hi, rq * 32 + 32);
+      for (int rr = a; rr < b; ++rr)
+        m2 = bf16x2_absmax(m2, *reinterpret_cast<const uint32_t*>(s_tile + rr * kTQRowBytes + cp * 4));
+      s_part[rq][cp] = m2;
+    }
+    __syncthreads();
+    if (tid < kTQCols / 2) {
+      uint32_t m2 = s_part[0][tid];
+#pragma unroll
+      for (int i = 1; i < 4; ++i) m2 = bf16x2_absmax(m2, s_part[i][tid]);
+      const float s0 = __fdiv_rn(fmaxf(bf16lo_to_f32(m2), kEps), kE4m3Max);
+      const float s1 = __fdiv_rn(fmaxf(bf16hi_to_f32(m2), kEps), kE4m3Max);
+      s_scale[2 * tid] = s0;
+      s_scale[2 * tid + 1] = s1;
+      if (2 * tid < ncols) {
+        so[c0 + 2 * tid] = s0;
+        so[c0 + 2 * tid + 1] = s1;
       }
-      *reinterpret_cast<uint2*>(qo + (int64_t)r * C + c0) = o;
     }
+    __syncthreads();
+    // cast: every slot row is written, rows outside the segment as zeros
+    if (pin) {
+      float sc[8], rc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j] = s_scale[piece * 8 + j];
+        rc[j] = __frcp_rn(sc[j]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = prow + 16 * i;
+        uint2 o = make_uint2(0u, 0u);
+        if (rr >= lo && rr < hi) {
+          const uint4 x = *reinterpret_cast<const uint4*>(s_tile + rr * kTQRowBytes + piece * 16);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint16_t c[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            c[j] = f32x2_to_e4m3x2(e4m3_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
+                                   e4m3_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+          o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+          o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+        }
+        *reinterpret_cast<uint2*>(qo + (int64_t)rr * C + c0 + piece * 8) = o;
+      }
+    }
+    __syncthreads();   // the tile and scales are reused by the next unit
   }
 }
 
@@ -276,8 +365,8 @@ cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
                                               int num_sms, int report, cudaStream_t s) {
   using namespace fp8moe;
-  int grid = num_sms * 8;
-  tgmm_quantize_tiles_kernel<<<grid, 256, 0, s>>>(
+  int grid = num_sms * 6;
+  tgmm_quantize_tiles_kernel<<<grid, kTQThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(lhs), static_cast<const __nv_bfloat16*>(dout), M, K, N,
       gs, E, Smax, qx, sx, qd, sd, report);
   return cudaGetLastError();

@@ -21,13 +21,15 @@
 //               ring that the rescale warps release.
 //   warp 1      tcgen05.mma kind::f8f6f4, M=128 (k), N=128 (n), K=32 rows, four
 //               per segment, into one of two TMEM partial buffers.
-//   warps 2..9  rescale: each thread owns one k row and 64 n columns of the
-//               f32 accumulator in registers, acc += (sx * sd[n]) * P[n]; at
-//               the end of the unit the accumulator goes to dW through a
-//               per-warp shared-memory transpose (128-byte coalesced stores).
-// The 128-wide n tile keeps the accumulator in registers (Blackwell allocates
-// registers per group of four warps, so this 10-warp CTA is budgeted as 12
-// warps) and matches the rescale work per segment to the MMA time.
+//   warps 2..17 rescale: each thread owns one k row and 32 n columns of the
+//               f32 accumulator in registers, acc += (sx * sd[n]) * P[n]; the
+//               partial products sit in four TMEM buffers so the MMA runs up
+//               to four segments ahead. At the end of the unit the accumulator
+//               goes to dW through a per-warp shared-memory transpose
+//               (128-byte coalesced stores).
+// The 128-wide n tile and four rescale warps per SM sub-partition keep the
+// accumulator in registers (Blackwell budgets registers per group of four warps)
+// and give the rescale enough warps to hide the TMEM and shared-memory latency.
 // An expert without rows writes zeros.
 #include <cstdint>
 #include <cuda.h>
@@ -46,17 +48,19 @@ constexpr int kStages = 4;
 constexpr int kXBytes = 128 * 128;
 constexpr int kDBytes = 128 * 128;
 constexpr int kStageBytes = kXBytes + kDBytes;    // 32 KB
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;    // 320
+constexpr int kEpiWarps = 16;                     // 4 per TMEM lane quarter
+constexpr int kCols = kBN * 4 / kEpiWarps;        // 32 accumulator columns per thread
+constexpr int kTBufs = 4;                         // TMEM partial buffers of kBN columns
+constexpr int kThreads = (2 + kEpiWarps) * 32;    // 576
 constexpr int kTmemCols = 512;
 constexpr int kXpose = 32 * 32 * 4;               // per-warp transpose buffer
-constexpr int kSRing = 4;                         // scale ring slots
+constexpr int kSRing = 16;                        // scale ring slots (1 KB each)
 
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[kTBufs];
+  uint64_t tempty[kTBufs];
   uint64_t sfull[kSRing];
   uint64_t sempty[kSRing];
   uint64_t drain;
@@ -114,13 +118,14 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
       }
-      for (int i = 0; i < 2; ++i) {
+      // released by one elected lane per rescale warp
+      for (int i = 0; i < kTBufs; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], kEpiWarps * 32);
+        mbar_init(&s.tempty[i], kEpiWarps);
       }
       for (int i = 0; i < kSRing; ++i) {
         mbar_init(&s.sfull[i], 1);
-        mbar_init(&s.sempty[i], kEpiWarps * 32);
+        mbar_init(&s.sempty[i], kEpiWarps);
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -207,8 +212,7 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
           mma_commit(&s.empty[st]);
           mma_commit(&s.tfull[acc]);
           if (++st == kStages) { st = 0; ph ^= 1; }
-          acc ^= 1;
-          if (acc == 0) aph ^= 1;
+          if (++acc == kTBufs) { acc = 0; aph ^= 1; }
         }
       }
       mma_commit(&s.drain);
@@ -216,9 +220,9 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     }
   } else {
     // ============================ rescale + store ===========================
-    const int ew = warp - 2;                 // 0..7
+    const int ew = warp - 2;                 // 0..15
     const int quarter = warp & 3;            // TMEM lanes 32*quarter ..
-    const int half = ew >> 2;                // columns [64*half, 64*half + 64)
+    const int cg = ew >> 2;                  // columns [kCols*cg, kCols*cg + kCols)
     const int r = quarter * 32 + lane;       // k row inside the tile
     float* xp = xpose + ew * (kXpose / 4);
     int acc = 0;
@@ -229,9 +233,9 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
       const int e = u / units_per_e, rem = u - e * units_per_e;
       const int kt = rem / nnt, ntile = rem - kt * nnt;
       const int q0 = s.segbase[e], q1 = s.segbase[e + 1];
-      float a[64];
+      float a[kCols];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) a[i] = 0.0f;
+      for (int i = 0; i < kCols; ++i) a[i] = 0.0f;
       for (int q = q0; q < q1; ++q) {
         const int ss = (int)(used % kSRing);
         if (!mbar_wait_warp(&s.sfull[ss], (uint32_t)((used / kSRing) & 1), kWhereEpilogue) ||
@@ -240,56 +244,49 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + cg * kCols), v);
         const float sxk = s.sring[ss][0][r];
-        const float4* sdv = reinterpret_cast<const float4*>(&s.sring[ss][1][half * 64]);
-        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + half * 64);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = sdv[(c * 32 + i) >> 2];
-            a[c * 32 + i] = __fmaf_rn(__fmul_rn(sxk, d4.x), __uint_as_float(v[i]), a[c * 32 + i]);
-            a[c * 32 + i + 1] = __fmaf_rn(__fmul_rn(sxk, d4.y), __uint_as_float(v[i + 1]), a[c * 32 + i + 1]);
-            a[c * 32 + i + 2] = __fmaf_rn(__fmul_rn(sxk, d4.z), __uint_as_float(v[i + 2]), a[c * 32 + i + 2]);
-            a[c * 32 + i + 3] = __fmaf_rn(__fmul_rn(sxk, d4.w), __uint_as_float(v[i + 3]), a[c * 32 + i + 3]);
-          }
-        }
+        const float4* sdv = reinterpret_cast<const float4*>(&s.sring[ss][1][cg * kCols]);
+        tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&s.tempty[acc]);
-        mbar_arrive(&s.sempty[ss]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.tempty[acc]);   // TMEM buffer free once in registers
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i) {
+          const float4 d4 = sdv[i];
+          a[4 * i] = __fmaf_rn(__fmul_rn(sxk, d4.x), __uint_as_float(v[4 * i]), a[4 * i]);
+          a[4 * i + 1] = __fmaf_rn(__fmul_rn(sxk, d4.y), __uint_as_float(v[4 * i + 1]), a[4 * i + 1]);
+          a[4 * i + 2] = __fmaf_rn(__fmul_rn(sxk, d4.z), __uint_as_float(v[4 * i + 2]), a[4 * i + 2]);
+          a[4 * i + 3] = __fmaf_rn(__fmul_rn(sxk, d4.w), __uint_as_float(v[4 * i + 3]), a[4 * i + 3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sempty[ss]);
         ++used;
-        acc ^= 1;
-        if (acc == 0) aph ^= 1;
+        if (++acc == kTBufs) { acc = 0; aph ^= 1; }
       }
       if (failed) break;
-      // store: 2 chunks of [32 k rows x 32 n] through the per-warp transpose
-      // buffer (16-byte chunk c4 of row i stored at chunk c4 ^ (i & 7)).
+      // store the [32 k rows x 32 n] block through the per-warp transpose buffer
+      // (16-byte chunk c4 of row i stored at chunk c4 ^ (i & 7)).
       const int k_warp0 = kt * kBK + quarter * 32;
-      const int n_half0 = ntile * kBN + half * 64;
+      const int n_cg0 = ntile * kBN + cg * kCols;
+      __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        __syncwarp();
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const int pc = c4 ^ (lane & 7);
-          *reinterpret_cast<float4*>(xp + lane * 32 + pc * 4) =
-              make_float4(a[c * 32 + c4 * 4], a[c * 32 + c4 * 4 + 1], a[c * 32 + c4 * 4 + 2],
-                          a[c * 32 + c4 * 4 + 3]);
-        }
-        __syncwarp();
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const int pc = c4 ^ (lane & 7);
+        *reinterpret_cast<float4*>(xp + lane * 32 + pc * 4) =
+            make_float4(a[c4 * 4], a[c4 * 4 + 1], a[c4 * 4 + 2], a[c4 * 4 + 3]);
+      }
+      __syncwarp();
 #pragma unroll 1
-        for (int it = 0; it < 8; ++it) {
-          const int i = it * 4 + (lane >> 3);       // row within the 32-row block
-          const int c4 = lane & 7;
-          const float4 v = *reinterpret_cast<const float4*>(xp + i * 32 + ((c4 ^ (i & 7)) * 4));
-          const int kk = k_warp0 + i;
-          const int nn = n_half0 + c * 32 + c4 * 4;
-          if (kk < K && nn < N)   // N % 16 == 0: a 4-column group is all in or all out
-            *reinterpret_cast<float4*>(dW + ((int64_t)e * K + kk) * N + nn) = v;
-        }
+      for (int it = 0; it < 8; ++it) {
+        const int i = it * 4 + (lane >> 3);       // row within the 32-row block
+        const int c4 = lane & 7;
+        const float4 v = *reinterpret_cast<const float4*>(xp + i * 32 + ((c4 ^ (i & 7)) * 4));
+        const int kk = k_warp0 + i;
+        const int nn = n_cg0 + c4 * 4;
+        if (kk < K && nn < N)   // N % 16 == 0: a 4-column group is all in or all out
+          *reinterpret_cast<float4*>(dW + ((int64_t)e * K + kk) * N + nn) = v;
       }
     }
   }

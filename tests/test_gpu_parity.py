@@ -224,3 +224,51 @@ def test_bf16_gmm_vs_float64(orc, swiglu):
     if swiglu:
         ref = torch.nn.functional.silu(ref[:, :N // 2]) * ref[:, N // 2:]
     check_bf16(out[:T], ref[:T], what="bf16 gmm")
+
+
+def _quotient_stress_rows(n_rows=2048, seed=17):
+    """Row r holds every bf16 value within 12 binades below a random amax (both
+    signs), so x / scale sweeps every e4m3 rounding boundary for 2048 scales."""
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for r in range(n_rows):
+        e = int(torch.randint(-20, 20, (1,), generator=g))
+        mant = int(torch.randint(0, 128, (1,), generator=g))
+        amax_bits = ((e + 127) << 7) | mant
+        lo_bits = ((e - 12 + 127) << 7)
+        mags = torch.arange(lo_bits, amax_bits + 1, dtype=torch.int32)
+        vals = torch.cat([mags, mags | 0x8000]).to(torch.int16)
+        rows.append(vals)
+    K = max(v.numel() for v in rows)
+    K = (K + 15) // 16 * 16
+    out = torch.zeros(n_rows, K, dtype=torch.int16)
+    for r, v in enumerate(rows):
+        out[r, :v.numel()] = v[torch.randperm(v.numel(), generator=g)]
+    return out.view(torch.bfloat16)
+
+
+def test_quantize_quotient_stress_bit_exact(orc):
+    x = _quotient_stress_rows()
+    M, K = x.shape
+    gs = torch.tensor([M], dtype=torch.int32)
+    q, sx = fb.quantize_rows(*cuda(x, gs))
+    q_ref, sx_ref, bad = orc.quantize_rows(x, gs)
+    assert bad == 0
+    assert torch.equal(sx.cpu(), sx_ref)
+    assert torch.equal(q.cpu(), q_ref)
+
+
+def test_tgmm_quantize_quotient_stress_bit_exact(orc):
+    """The same values laid out down the columns of 128-row tiles."""
+    x = _quotient_stress_rows(n_rows=256, seed=18)          # [256, K]
+    cols = x.view(torch.int16)[:, :1024].reshape(256, 1024)
+    lhs = cols.t().contiguous().view(torch.bfloat16)        # [1024 rows, 256 cols]
+    lhs = lhs[:, :256].contiguous()
+    M = lhs.shape[0]
+    dout = W.cotangent(M, 64, 3)
+    gs = torch.tensor([300, 500, 224], dtype=torch.int32)
+    qx, sxt, qd, sd = fb.tgmm_quantize_tiles(*cuda(lhs, dout, gs))
+    rqx, rsx, rqd, rsd, nseg, bad = orc.tgmm_quantize_tiles(lhs, dout, gs)
+    assert bad == 0
+    assert torch.equal(sxt.cpu()[:nseg], rsx[:nseg]) and torch.equal(qx.cpu()[:nseg], rqx[:nseg])
+    assert torch.equal(sd.cpu()[:nseg], rsd[:nseg]) and torch.equal(qd.cpu()[:nseg], rqd[:nseg])
