@@ -1,4 +1,4 @@
-// gmm_fwd.cu -- ragged grouped matmul forward on tcgen05 tensor cores.
+// gmm_fwd.cu -- ragged grouped matmul forward on tcgen05 tensor cores, CTA pairs.
 //
 //   out[m, n] = sx[m] * sw[e(m), n] * sum_k qx[m, k] * qw[e(m), k, n]       (FP8 arm)
 //   out[m, j] = silu(g) * u, g = y[m, j], u = y[m, N/2 + j]                  (SwiGLU)
@@ -11,21 +11,26 @@
 // grouped matmul used as the fake-QAT comparison arm ("... Tests": the BF16 GMM
 // gets a weight dequantized beforehand).
 //
-// Design (one CTA per SM, persistent):
-//   warp 0      TMA producer: A tile [128 rows x 128 bytes of K] (K-major,
-//               128-byte swizzle) and the B tile, 256 columns of the
-//               N-contiguous weight by 128 bytes of K (MN-major, 128-byte
-//               swizzle); 4-stage ring of 48 KB stages.
-//   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators) and
-//               the single thread that issues tcgen05.mma (M=128, N=256).
-//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator, scales,
-//               SwiGLU, bf16 rounding, row-masked 16-byte stores. The second
-//               accumulator lets the next tile's MMAs run meanwhile.
-// Work units are (expert, 128-row m tile, 256-column n tile), enumerated expert
-// by expert, n tile by n tile, m tiles fastest, so that concurrently running
-// CTAs share weight tiles through L2. Each CTA derives the ragged layout from
-// group_sizes itself; tiles begin at their group's first row and rows past the
-// group end are computed but never stored.
+// Design: persistent clusters of two CTAs (one CTA per SM). A work unit is
+// (expert, pair of 128-row m tiles, 256-column n tile); the pair computes the
+// 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256, N = 256) issued by the
+// even CTA. Each CTA loads only its own 128 A rows and one 128-column half of
+// the B tile, so a CTA moves 32 KB per 128-byte K step instead of the 48 KB a
+// single-CTA 128 x 256 tile needs: the tensor cores stay fed from L2.
+//   warp 0      TMA producer of this CTA's A rows (K-major, 128-byte swizzle)
+//               and B half (MN-major, 128-byte swizzle), 6 stages of 32 KB;
+//               completion is counted on the even CTA's barrier.
+//   warp 1      TMEM allocation for the pair (512 columns = two 128 x 256 f32
+//               accumulators per CTA); in the even CTA, the MMA-issuing thread.
+//   warps 2..5  epilogue of this CTA's 128 rows: tcgen05.ld, scales, SwiGLU,
+//               bf16, row-masked 16-byte stores; the second accumulator lets
+//               the next tile's MMAs run meanwhile.
+// SwiGLU: the even CTA's B half is the gate columns, the odd CTA's the matching
+// up columns, so accumulator columns [0, 128) are gate and [128, 256) up.
+// Units are enumerated expert by expert, n tile by n tile, pairs fastest, so
+// that concurrently running clusters share weight tiles through L2. Each CTA
+// derives the ragged layout from group_sizes itself; tiles begin at their
+// group's first row and rows past the group end are computed but never stored.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -38,25 +43,24 @@
 namespace fp8moe {
 namespace fwd {
 
-constexpr int kStages = 4;
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kABytes = kBM * 128;          // 16 KB
-constexpr int kBBytes = kBN * 128;          // 32 KB: 256 columns x 128 bytes of K
+constexpr int kStages = 6;
+constexpr int kBM = 128;                    // rows per CTA (M = 256 per pair)
+constexpr int kBN = 256;                    // accumulator columns (MMA N)
+constexpr int kABytes = kBM * 128;          // 16 KB: 128 rows x 128 bytes of K
+constexpr int kBBytes = 128 * 128;          // 16 KB: this CTA's 128 columns x 128 bytes of K
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[kStages];      // even CTA: both CTAs' tiles of the stage landed
+  uint64_t empty[kStages];     // both CTAs: the stage's MMAs completed
+  uint64_t tfull[2];           // both CTAs: accumulator ready
+  uint64_t tempty[2];          // even CTA: both CTAs' epilogues drained it
   uint64_t drain;
   uint32_t tmem_base;
   int32_t T;
   int32_t total_units;
-  int32_t abort_flag;
   float sw[2][kBN];
   int32_t begin[kMaxExperts];
   int32_t end[kMaxExperts];
@@ -71,23 +75,24 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
 }
 
 struct Unit {
-  int e, row0, rows, j;
+  int e, row0, rows, j;   // row0 / rows: this CTA's m tile (rows may be <= 0)
 };
 
-__device__ __forceinline__ Unit decode_unit(const Smem& s, int E, int nt, int u) {
+__device__ __forceinline__ Unit decode_unit(const Smem& s, int E, int nt, int u, int rank) {
   Unit r;
   r.e = find_bucket(s.prefix, E, u);
   const int mt = (s.end[r.e] - s.begin[r.e] + kBM - 1) / kBM;
+  const int mtp = (mt + 1) / 2;
   const int local = u - s.prefix[r.e];
-  r.j = local / mt;
-  const int i = local - r.j * mt;
-  r.row0 = s.begin[r.e] + i * kBM;
+  r.j = local / mtp;
+  const int p = local - r.j * mtp;
+  r.row0 = s.begin[r.e] + (2 * p + rank) * kBM;
   r.rows = min(kBM, s.end[r.e] - r.row0);
   return r;
 }
 
-// FP8: operands are 1 byte, a 128-byte swizzle row holds 128 K values of A (or
-// 128 N values of B); BF16: 64.
+// FP8: a 128-byte swizzle row holds 128 K values of A (or 128 N values of B);
+// BF16: 64.
 template <bool FP8, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -99,13 +104,15 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                               ~uintptr_t(1023));
   Smem& s = *reinterpret_cast<Smem*>(tiles + (size_t)kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
 
   constexpr int kElemsPerRow = FP8 ? 128 : 64;        // elements per 128-byte row
   const int Nout = SWIGLU ? N / 2 : N;
   const int nt = SWIGLU ? (Nout + 127) / 128 : (N + kBN - 1) / kBN;
   const int nkb = (K + kElemsPerRow - 1) / kElemsPerRow;
 
-  // ---- set-up: ragged layout, unit prefix, barriers, TMEM
+  // ---- set-up: ragged layout, unit prefix (units = m-tile pairs), barriers, TMEM
   if (warp == 0) {
     load_groups_warp0(gs, E, M, s.begin, s.end, &s.T, blockIdx.x == 0);
     __syncwarp();
@@ -113,7 +120,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int base = 0; base < E; base += 32) {
       int e = base + lane;
       int32_t n = 0;
-      if (e < E) n = ((s.end[e] - s.begin[e] + kBM - 1) / kBM) * nt;
+      if (e < E) n = (((s.end[e] - s.begin[e] + kBM - 1) / kBM + 1) / 2) * nt;
       int32_t incl = n;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -126,7 +133,6 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       s.prefix[E] = carry;
       s.total_units = carry;
-      s.abort_flag = 0;
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
     }
@@ -138,17 +144,18 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 4);   // one elected lane per epilogue warp
+        mbar_init(&s.tempty[i], 8);   // one elected lane per epilogue warp, both CTAs
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
     }
     __syncwarp();
-    tmem_alloc(&s.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&s.tmem_base, kTmemCols);
+    tmem_relinquish_pair();
     tc_fence_before();
   }
   __syncthreads();
+  cluster_sync();      // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const int total = s.total_units;
   const uint32_t tmem = s.tmem_base;
@@ -160,47 +167,47 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = decode_unit(s, E, nt, u);
-        int nb0, nb1;
-        if (SWIGLU) { nb0 = t.j * 128; nb1 = Nout + t.j * 128; }
-        else { nb0 = t.j * kBN; nb1 = t.j * kBN + 128; }
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        const Unit t = decode_unit(s, E, nt, u, rank);
+        int nb;
+        if (SWIGLU) nb = (rank ? Nout : 0) + t.j * 128;
+        else nb = t.j * kBN + rank * 128;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&s.empty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.full[st], kStageBytes);
+          if (!mbar_wait_cluster(&s.empty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
+          // the even CTA's barrier counts the bytes of both CTAs
+          if (rank == 0) mbar_arrive_expect_tx(&s.full[st], 2 * kStageBytes);
+          const uint32_t bar = mapa_shared(smem_u32(&s.full[st]), 0);
           uint8_t* a = tiles + st * kStageBytes;
           uint8_t* b = a + kABytes;
           const int k0 = kb * kElemsPerRow;
-          tma_load_2d(a, &tmA, &s.full[st], k0, t.row0);
+          tma_load_2d_pair(a, &tmA, bar, k0, t.row0);
           if (FP8) {
-            tma_load_3d(b, &tmB, &s.full[st], nb0, k0, t.e);
-            tma_load_3d(b + 16384, &tmB, &s.full[st], nb1, k0, t.e);
+            tma_load_3d_pair(b, &tmB, bar, nb, k0, t.e);
           } else {
-            // bf16: four 64-column boxes of 64 K rows (8 KB each)
-            tma_load_3d(b, &tmB, &s.full[st], nb0, k0, t.e);
-            tma_load_3d(b + 8192, &tmB, &s.full[st], nb0 + 64, k0, t.e);
-            tma_load_3d(b + 16384, &tmB, &s.full[st], nb1, k0, t.e);
-            tma_load_3d(b + 24576, &tmB, &s.full[st], nb1 + 64, k0, t.e);
+            // bf16: two 64-column boxes of 64 K rows (8 KB each)
+            tma_load_3d_pair(b, &tmB, bar, nb, k0, t.e);
+            tma_load_3d_pair(b + 8192, &tmB, bar, nb + 64, k0, t.e);
           }
           ++issued;
           if (++st == kStages) { st = 0; ph ^= 1; }
         }
       }
-      if (!ok) s.abort_flag = 1;
-      // drain: every load issued must have landed before the CTA may exit
-      int64_t n_last = issued < kStages ? issued : kStages;
-      for (int64_t i = 1; i <= n_last; ++i) {
-        int64_t idx = issued - i;
-        mbar_wait(&s.full[idx % kStages], (uint32_t)((idx / kStages) & 1), kWhereDrain);
+      // drain (even CTA): every load of both CTAs landed before either may exit
+      if (rank == 0) {
+        int64_t n_last = issued < kStages ? issued : kStages;
+        for (int64_t i = 1; i <= n_last; ++i) {
+          int64_t idx = issued - i;
+          mbar_wait_cluster(&s.full[idx % kStages], (uint32_t)((idx / kStages) & 1), kWhereDrain);
+        }
       }
     }
   } else if (warp == 1) {
     // ============================== MMA issuer ============================
-    if (lane == 0) {
-      constexpr uint32_t idesc = FP8 ? make_idesc(0, 0, 0, 1, kBM, kBN)
-                                     : make_idesc(1, 1, 0, 1, kBM, kBN);
-      // B (MN-major): atoms of 128 bytes along N; FP8 atom = 128 columns with
-      // the second half 16 KB further; BF16 atom = 64 columns, 8 KB apart.
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = FP8 ? make_idesc(0, 0, 0, 1, 2 * kBM, kBN)
+                                     : make_idesc(1, 1, 0, 1, 2 * kBM, kBN);
+      // B (MN-major), this CTA's 128 columns: FP8 one 128-column atom; BF16
+      // two 64-column atoms 8 KB apart.
       constexpr uint32_t kBLbo = FP8 ? 16384 : 8192;
       // one MMA consumes 32 bytes of K: FP8 32 K values (= 32 B-rows), BF16 16
       constexpr uint32_t kBStep = FP8 ? 32 * 128 : 16 * 128;
@@ -209,12 +216,12 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        if (!mbar_wait(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        if (!mbar_wait_cluster(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * kBN);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&s.full[st], ph, kWhereMma)) { ok = false; break; }
+          if (!mbar_wait_cluster(&s.full[st], ph, kWhereMma)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(tiles + st * kStageBytes);
           const uint32_t b_addr = a_addr + kABytes;
@@ -222,35 +229,34 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = make_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = make_desc(b_addr + kk * kBStep, kBLbo, 1024, kSwizzle128B);
-            if (FP8) mma_f8f6f4(d, ad, bd, idesc, (kb | kk) != 0);
-            else mma_f16(d, ad, bd, idesc, (kb | kk) != 0);
+            if (FP8) mma_f8f6f4_pair(d, ad, bd, idesc, (kb | kk) != 0);
+            else mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0);
           }
-          mma_commit(&s.empty[st]);
+          mma_commit_pair(&s.empty[st]);
           if (++st == kStages) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
-        mma_commit(&s.tfull[acc]);
+        mma_commit_pair(&s.tfull[acc]);
         acc ^= 1;
         if (acc == 0) aph ^= 1;
       }
-      if (!ok) s.abort_flag = 1;
-      // all MMAs of this thread complete before TMEM may be released
-      mma_commit(&s.drain);
-      mbar_wait(&s.drain, 0, kWhereDrain);
+      // all MMAs complete (in both CTAs' TMEM) before TMEM may be released
+      mma_commit_pair(&s.drain);
     }
+    if (lane == 0) mbar_wait_cluster(&s.drain, 0, kWhereDrain);
   } else {
     // =============================== epilogue =============================
     const int et = threadIdx.x - 64;                 // 0..127
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter ..
-    const int r = quarter * 32 + lane;               // row inside the tile
+    const int r = quarter * 32 + lane;               // row inside this CTA's tile
     int acc = 0;
     uint32_t aph = 0;
     int sb = 0;
-    // A timed-out wait marks the thread failed; it keeps iterating (without
+    // A timed-out wait marks the warp failed; it keeps iterating (without
     // touching TMEM) so that every epilogue thread passes the same named barriers.
     bool failed = false;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit t = decode_unit(s, E, nt, u);
+    for (int u = cluster; u < total; u += nclusters) {
+      const Unit t = decode_unit(s, E, nt, u, rank);
       // per-column scales of this tile's 256 accumulator columns
       if (FP8) {
 #pragma unroll
@@ -272,7 +278,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool row_ok = r < t.rows;
       const int64_t row = (int64_t)t.row0 + r;
       const float sxr = (FP8 && row_ok) ? __ldg(sx + row) : 1.0f;
-      if (!failed && !mbar_wait_warp(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
+      if (!failed && !mbar_wait_warp_cluster(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
       if (failed) {
         acc ^= 1;
         if (acc == 0) aph ^= 1;
@@ -280,66 +286,69 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         continue;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
-      __nv_bfloat16* orow = out + row * Nout;
-      constexpr int kChunks = SWIGLU ? 4 : 8;
+      if (t.rows > 0) {
+        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+        __nv_bfloat16* orow = out + row * Nout;
+        constexpr int kChunks = SWIGLU ? 4 : 8;
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
-        uint32_t o[16];
-        int col0;
-        if (SWIGLU) {
-          uint32_t g[32], v[32];
-          tmem_ld32(tbase + c * 32, g);
-          tmem_ld32(tbase + 128 + c * 32, v);
-          tmem_ld_wait();
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t o[16];
+          int col0;
+          if (SWIGLU) {
+            uint32_t g[32], v[32];
+            tmem_ld32(tbase + c * 32, g);
+            tmem_ld32(tbase + 128 + c * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y[2];
+            for (int i = 0; i < 32; i += 2) {
+              float y[2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              float gg = __uint_as_float(g[i + h]);
-              float uu = __uint_as_float(v[i + h]);
-              if (FP8) {
-                gg = __fmul_rn(__fmul_rn(gg, sxr), s.sw[sb][c * 32 + i + h]);
-                uu = __fmul_rn(__fmul_rn(uu, sxr), s.sw[sb][128 + c * 32 + i + h]);
+              for (int h = 0; h < 2; ++h) {
+                float gg = __uint_as_float(g[i + h]);
+                float uu = __uint_as_float(v[i + h]);
+                if (FP8) {
+                  gg = __fmul_rn(__fmul_rn(gg, sxr), s.sw[sb][c * 32 + i + h]);
+                  uu = __fmul_rn(__fmul_rn(uu, sxr), s.sw[sb][128 + c * 32 + i + h]);
+                }
+                const float sg = __fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg)));
+                y[h] = __fmul_rn(sg, uu);
               }
-              const float sg = __fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg)));
-              y[h] = __fmul_rn(sg, uu);
+              o[i / 2] = f32x2_to_bf16x2(y[0], y[1]);
             }
-            o[i / 2] = f32x2_to_bf16x2(y[0], y[1]);
-          }
-          col0 = t.j * 128 + c * 32;
-        } else {
-          uint32_t v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0 = __uint_as_float(v[i]), y1 = __uint_as_float(v[i + 1]);
-            if (FP8) {
-              y0 = __fmul_rn(__fmul_rn(y0, sxr), s.sw[sb][c * 32 + i]);
-              y1 = __fmul_rn(__fmul_rn(y1, sxr), s.sw[sb][c * 32 + i + 1]);
-            }
-            o[i / 2] = f32x2_to_bf16x2(y0, y1);
-          }
-          col0 = t.j * kBN + c * 32;
-        }
-        if (row_ok) {
-          if (col0 + 32 <= Nout) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            col0 = t.j * 128 + c * 32;
           } else {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (col0 + q < Nout) dst[col0 + q] = (uint16_t)(o[q / 2] >> (16 * (q & 1)));
+            for (int i = 0; i < 32; i += 2) {
+              float y0 = __uint_as_float(v[i]), y1 = __uint_as_float(v[i + 1]);
+              if (FP8) {
+                y0 = __fmul_rn(__fmul_rn(y0, sxr), s.sw[sb][c * 32 + i]);
+                y1 = __fmul_rn(__fmul_rn(y1, sxr), s.sw[sb][c * 32 + i + 1]);
+              }
+              o[i / 2] = f32x2_to_bf16x2(y0, y1);
+            }
+            col0 = t.j * kBN + c * 32;
+          }
+          if (row_ok) {
+            if (col0 + 32 <= Nout) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + col0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            } else {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                if (col0 + q < Nout) dst[col0 + q] = (uint16_t)(o[q / 2] >> (16 * (q & 1)));
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+      // the even CTA's MMA thread waits for the epilogue warps of both CTAs
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) aph ^= 1;
       sb ^= 1;
@@ -347,9 +356,10 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 
   __syncthreads();
+  cluster_sync();      // both CTAs done with TMEM, shared memory and barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -359,9 +369,21 @@ cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, kThreads, kSmemBytes, s>>>(a.tmA, a.tmB, a.sx, a.scale, a.gs,
-                                             static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N,
-                                             a.E);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);   // whole CTA pairs, one CTA per SM
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sx, a.scale, a.gs,
+                           static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N, a.E);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
