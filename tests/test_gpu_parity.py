@@ -192,6 +192,32 @@ def test_tgmm_vs_oracle(orc, M, K, N, E, gs):
                 assert (dw[e] == 0).all()
 
 
+def test_tgmm_odd_segments_ragged_tiles_and_16b_aligned_out(orc):
+    """Experts with an odd number of 128-row segments (a pipeline stage then
+    carries one live segment), k and n tiles cut by K = 272 and N = 144, and a dW
+    that is 16- but not 32-byte aligned (the kernel's narrower store path); the
+    same call on an aligned dW must give the same bits."""
+    M, K, N = 1280, 272, 144
+    gs = torch.tensor([300, 400, 0, 400], dtype=torch.int32)   # 3, 4, 0, 4 segments
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=31), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=32), T)
+    xg, dg, gsg = cuda(x, d, gs)
+    E = gs.numel()
+    buf = torch.full((E * K * N + 4,), 5.0, dtype=torch.float32, device=DEV)
+    out = buf[4:].view(E, K, N)
+    assert out.data_ptr() % 32 == 16
+    dw = fb.tgmm_drhs_quant(xg, dg, gsg, out=out)
+    ref, bad = orc.tgmm(x, d, gs)
+    assert bad == 0
+    check_f32_rel(dw, ref, what="tgmm odd/ragged")
+    assert (dw[2] == 0).all()
+    assert (buf[:4] == 5.0).all()
+    dw2 = fb.tgmm_drhs_quant(xg, dg, gsg)
+    assert dw2.data_ptr() % 32 == 0
+    assert torch.equal(dw2, dw)
+
+
 def test_tgmm_quantize_tiles_bit_exact(orc):
     M, K, N = 1024, 512, 256
     gs = torch.tensor([300, 0, 129, 1, 200, 0], dtype=torch.int32)
