@@ -40,6 +40,14 @@ E, HID, FF, TOKENS, TOPK = 32, 7168, 2048, 4096, 8
 M = TOKENS * TOPK
 ROWS_PER_EXPERT = M // E
 METRIC = "FP8 GMM TFLOP/s (wi+SwiGLU fwd, wo fwd, dLHS) and % of GB300 FP8 peak"
+# DRAM bytes (read + write) of one wi forward call at 32 experts x 1024 rows,
+# K = 7168, N = 4096: quantize_rows_kernel<4> 469.8 + 202.9 MB and
+# gmm_fwd_kernel<1, 1> 1194.6 + 124.0 MB, from a one-pass ncu capture
+# (dram__bytes_read.sum, dram__bytes_write.sum) of this bench's workload.
+# Valid for those two kernels as captured; set to None when either changes.
+WI_FWD_TRAFFIC = 1991.3e6
+WI_FWD_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi forward "
+                         "(row quantizer + GMM), profiles/gmm_fwd_wi_e4_m4096_k7168_n4096.md")
 
 
 def step_flops(T: int) -> dict:
@@ -449,7 +457,8 @@ def main():
             "roofline": {"kernel": "wi fwd (row quantize + FP8 GMM + SwiGLU)", "bound": "tensor",
                          "achieved": round(wi_tflops, 1), "peak": round(fp8_peak, 1),
                          "unit": "TFLOP/s", "frac": round(wi_tflops / fp8_peak, 3),
-                         "traffic": None,
+                         "traffic": WI_FWD_TRAFFIC if E == 32 else None,
+                         "traffic_source": WI_FWD_TRAFFIC_SOURCE if E == 32 else None,
                          "peak_source": f"{pk['source']} bf16 x2 (fp8/bf16 nominal ratio), burst"},
             "kernels": kern, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, **extra,
         }
