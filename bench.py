@@ -178,6 +178,47 @@ class Step:
             ev[5].record()
 
 
+def microbench(fb, timeit, dev) -> dict:
+    """FP8 vs BF16 forward GMMs at the kernel microbenchmark shape of "MoE: native
+    FP8 QAT for routed-expert GMMs", section Tests: one call at full fill, 64
+    experts, 225,280 rows, hidden 4096, moe intermediate 1024. The BF16 arm gets
+    weights dequantized beforehand (untimed); the FP8 arm's time includes the
+    activation quantization. The pages report FP8 1.6-1.7x faster (TPU7x)."""
+    from fp8_moe_routed_gb300 import workloads as W
+    mb = W.MICROBENCH
+    gs = W.group_sizes(mb.routing, E=mb.E, M=mb.M).to(dev)
+    x = W.activations(mb.M, mb.K, 41, device=dev)
+    wi_c, wi_s = W.fp8_weights(mb.E, mb.K, 2 * mb.F, mb.sigma_wi, 42, device=dev)
+    wo_c, wo_s = W.fp8_weights(mb.E, mb.F, mb.K, mb.sigma_wo, 43, device=dev)
+    h = torch.empty(mb.M, mb.F, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(mb.M, mb.K, dtype=torch.bfloat16, device=dev)
+    ws_wi = torch.empty(fb.workspace_size(fb.OP_GMM_SILU_FP8_FWD, mb.M, mb.K, 2 * mb.F, mb.E),
+                        dtype=torch.uint8, device=dev)
+    ws_wo = torch.empty(fb.workspace_size(fb.OP_GMM_FP8_FWD, mb.M, mb.F, mb.K, mb.E),
+                        dtype=torch.uint8, device=dev)
+    wi_bf = fb.dequantize_fp8_codes(wi_c, wi_s)
+    wo_bf = fb.dequantize_fp8_codes(wo_c, wo_s)
+    t_wi = timeit(lambda: fb.gmm_silu_fp8_fwd(x, wi_c, wi_s, gs, out=h, workspace=ws_wi))
+    t_wo = timeit(lambda: fb.gmm_fp8_fwd(h, wo_c, wo_s, gs, out=y, workspace=ws_wo))
+    t_wi_bf = timeit(lambda: fb.gmm_bf16_fwd(x, wi_bf, gs, True, out=h))
+    t_wo_bf = timeit(lambda: fb.gmm_bf16_fwd(h, wo_bf, gs, False, out=y))
+    fl_wi = 2.0 * mb.M * mb.K * 2 * mb.F
+    fl_wo = 2.0 * mb.M * mb.F * mb.K
+    out = {"workload": "microbench_E64_M225280_K4096_F1024",
+           "wi_fp8_ms": round(t_wi, 4), "wi_bf16_ms": round(t_wi_bf, 4),
+           "wi_fp8_speedup": round(t_wi_bf / t_wi, 3),
+           "wi_fp8_tflops": round(fl_wi / (t_wi * 1e-3) / 1e12, 1),
+           "wi_bf16_tflops": round(fl_wi / (t_wi_bf * 1e-3) / 1e12, 1),
+           "wo_fp8_ms": round(t_wo, 4), "wo_bf16_ms": round(t_wo_bf, 4),
+           "wo_fp8_speedup": round(t_wo_bf / t_wo, 3),
+           "wo_fp8_tflops": round(fl_wo / (t_wo * 1e-3) / 1e12, 1),
+           "wo_bf16_tflops": round(fl_wo / (t_wo_bf * 1e-3) / 1e12, 1),
+           "pages_fp8_speedup": "1.6-1.7x (TPU7x, same comparison)"}
+    del x, wi_c, wo_c, wi_bf, wo_bf, h, y, ws_wi, ws_wo
+    torch.cuda.empty_cache()
+    return out
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -401,6 +442,7 @@ def main():
                                   "gbs": round(deq_bytes / (t_deq * 1e-3) / 1e9, 1),
                                   "frac_of_hbm": round(deq_bytes / (t_deq * 1e-3) / 1e9 / pk["hbm"], 3)}
         del w_bf, wo_bf
+        extra["microbench"] = microbench(fb, timeit, torch.device("cuda", torch.cuda.current_device()))
 
     # ------------------------------------------------------------------ e2e
     e2e = None

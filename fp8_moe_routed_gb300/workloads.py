@@ -26,6 +26,11 @@ not available, these synthetic draws stand in for it):
   in the tail rows.
 * ``sweep``: E=128, K=4096, N=1536 (wi 3072), M in {8192 .. 131072}, sizes
   uniform in [0, 2M/128] then adjusted by +-1 to sum to M.
+* ``microbench``: the kernel microbenchmark shape of "MoE: native FP8 QAT for
+  routed-expert GMMs", section Tests (one call at full fill, 64 experts,
+  225,280 rows, the Qwen3.5-397B-A17B per-device MLP: hidden 4096, moe
+  intermediate 1024, so wi is [64, 4096, 2048] and wo [64, 1024, 4096]);
+  full fill read as 225,280 / 64 = 3520 rows per expert.
 """
 from __future__ import annotations
 
@@ -80,6 +85,11 @@ def group_sizes(kind: str, seed: int = 0, E: Optional[int] = None,
     if kind == "balanced":
         E = E or 32
         M = M or 32768
+        assert M % E == 0
+        return torch.full((E,), M // E, dtype=torch.int32)
+    if kind == "full_fill":
+        E = E or 64
+        M = M or 225280
         assert M % E == 0
         return torch.full((E,), M // E, dtype=torch.int32)
     if kind in ("skewed", "dropless"):
@@ -183,6 +193,10 @@ SKEWED = Shapes("skewed", E=32, K=7168, F=2048, M=32768, routing="skewed",
                 sigma_wi=0.006, sigma_wo=0.006)
 DROPLESS = Shapes("dropless", E=32, K=7168, F=1024, M=65536, routing="dropless",
                   sigma_wi=0.006, sigma_wo=0.006)
+
+
+MICROBENCH = Shapes("microbench", E=64, K=4096, F=1024, M=225280, routing="full_fill",
+                    sigma_wi=0.02, sigma_wo=0.02)
 
 
 def sweep_shapes(M: int) -> Shapes:

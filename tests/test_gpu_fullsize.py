@@ -172,3 +172,38 @@ def test_sweep_forward_and_dlhs_paths(orc, M):
     ref_a, _, bad = orc.gmm_dlhs(d2.cpu(), c2.cpu(), s2.cpu(), gs, rows=rows_b)
     assert bad == 0
     check_bf16(a.cpu()[rows_b], ref_a[rows_b], what="sweep dlhs cached")
+
+
+def test_microbench_shape_forward_and_dlhs_sampled(orc):
+    """The pages' kernel microbenchmark shape (64 experts at full fill, 225,280
+    rows, hidden 4096, moe intermediate 1024; every expert ends in a partial
+    128-row tile): wi forward + SwiGLU and wo forward on sampled rows, both dLHS
+    GMMs on fewer rows."""
+    mb = W.MICROBENCH
+    gs = W.group_sizes(mb.routing, E=mb.E, M=mb.M)
+    gsd = gs.to(DEV)
+    x = W.activations(mb.M, mb.K, 51, device=DEV)
+    wi_c, wi_s = W.fp8_weights(mb.E, mb.K, 2 * mb.F, mb.sigma_wi, 52, device=DEV)
+    wo_c, wo_s = W.fp8_weights(mb.E, mb.F, mb.K, mb.sigma_wo, 53, device=DEV)
+    h = fb.gmm_silu_fp8_fwd(x, wi_c, wi_s, gsd)
+    y = fb.gmm_fp8_fwd(h, wo_c, wo_s, gsd)
+    rows = sample_rows(gs, 0, seed=9)[::3]
+    wi_cc, wi_sc, wo_cc, wo_sc = wi_c.cpu(), wi_s.cpu(), wo_c.cpu(), wo_s.cpu()
+    ref_h, _, bad = orc.gmm_fwd(x.cpu(), wi_cc, wi_sc, gs, silu=True, rows=rows)
+    assert bad == 0
+    check_bf16(h.cpu()[rows], ref_h[rows], what="microbench wi fwd")
+    ref_y, _, bad = orc.gmm_fwd(h.cpu(), wo_cc, wo_sc, gs, silu=False, rows=rows)
+    assert bad == 0
+    check_bf16(y.cpu()[rows], ref_y[rows], what="microbench wo fwd")
+    del x, y
+    dy = W.cotangent(mb.M, mb.K, 54, device=DEV)
+    dgu = W.cotangent(mb.M, 2 * mb.F, 55, device=DEV)
+    dh = fb.gmm_dlhs_fp8(dy, wo_c, wo_s, gsd)
+    dx = fb.gmm_dlhs_fp8(dgu, wi_c, wi_s, gsd)
+    rows_b = rows[:: max(1, len(rows) // 16)]
+    ref_dh, _, bad = orc.gmm_dlhs(dy.cpu(), wo_cc, wo_sc, gs, rows=rows_b)
+    assert bad == 0
+    check_bf16(dh.cpu()[rows_b], ref_dh[rows_b], what="microbench wo dlhs")
+    ref_dx, _, bad = orc.gmm_dlhs(dgu.cpu(), wi_cc, wi_sc, gs, rows=rows_b)
+    assert bad == 0
+    check_bf16(dx.cpu()[rows_b], ref_dx[rows_b], what="microbench wi dlhs")

@@ -22,6 +22,11 @@ def test_group_size_recipes():
         assert int(s.sum()) == M and s.min() >= 0 and s.max() <= 2 * M // 128
         assert (s % 128 != 0).any()
     assert torch.equal(W.group_sizes("sweep", seed=1, M=8192), W.group_sizes("sweep", seed=1, M=8192))
+    ff = W.group_sizes("full_fill")
+    assert ff.numel() == 64 and int(ff.sum()) == 225280 and (ff == 3520).all()
+    assert 3520 % 128 != 0          # every expert ends in a partial 128-row tile
+    mb = W.MICROBENCH
+    assert (mb.E, mb.K, mb.F, mb.M) == (64, 4096, 1024, 225280)
 
 
 def test_weights_are_valid_e4m3_with_channel_max():
