@@ -14,6 +14,9 @@
 //          gradient dtype" -- section What.
 //   [SM]  "Fix fp8 MoE on the sparse_matmul path" -- section Fix (names the
 //          forward dtype float8_e4m3fn).
+//   The SwiGLU backward (dSwiGLU) is the derivative of silu(g) * u written out;
+//   [NQ] Implementation names the op that fuses it into the wo GMM
+//   (gmm_dswiglu_fp8).
 //
 // Floating point: all sums are taken in double. Products of two e4m3 values are
 // multiples of 2^-18 with magnitude <= 448^2, so any sum of up to 2^17 of them is
@@ -348,6 +351,40 @@ int64_t orc_gmm_dlhs(const uint16_t* dout, int64_t M, int64_t N,
     }
   }
   return bad.load();
+}
+
+// ----- dSwiGLU (backward of the wi SwiGLU, fused into the wo dLHS) ------------
+// [NQ] Implementation: gmm_dswiglu_fp8 is the wo op; its backward is the wo dLHS
+// followed by the SwiGLU backward. With h = silu(g) * u, silu(z) = z * sig(z),
+// sig(z) = 1 / (1 + exp(-z)), and upstream dh = dL/dh:
+//   dg = dh * u * silu'(g),   silu'(g) = sig(g) * (1 + g * (1 - sig(g)))
+//   du = dh * silu(g)
+// g = gu[m, j], u = gu[m, F + j] (gate | up halves of the wi output, bf16); dh is
+// taken unrounded (double, e.g. the exact dLHS sum) and each result is rounded
+// once to bf16. dgu is [M, 2F] with dg in [0, F) and du in [F, 2F); rows as in
+// orc_gmm_fwd (nullptr = every row < M).
+void orc_dswiglu(const double* dh, const uint16_t* gu, int64_t M, int64_t F,
+                 const int64_t* rows, int64_t nrows, uint16_t* dgu, double* dgu_f64) {
+  std::vector<int64_t> all;
+  if (!rows) { all.resize(M); for (int64_t m = 0; m < M; ++m) all[m] = m; rows = all.data(); nrows = M; }
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < nrows; ++i) {
+    const int64_t m = rows[i];
+    for (int64_t j = 0; j < F; ++j) {
+      const double d = dh[m * F + j];
+      const double g = (double)bf16_to_f32(gu[m * 2 * F + j]);
+      const double u = (double)bf16_to_f32(gu[m * 2 * F + F + j]);
+      const double sg = 1.0 / (1.0 + std::exp(-g));
+      const double dg = d * u * (sg * (1.0 + g * (1.0 - sg)));
+      const double du = d * (g * sg);
+      dgu[m * 2 * F + j] = f64_to_bf16_rne(dg);
+      dgu[m * 2 * F + F + j] = f64_to_bf16_rne(du);
+      if (dgu_f64) {
+        dgu_f64[m * 2 * F + j] = dg;
+        dgu_f64[m * 2 * F + F + j] = du;
+      }
+    }
+  }
 }
 
 // ----- a7: tgmm operand quantization per gm-tile per channel -----------------

@@ -57,6 +57,8 @@ def lib():
             L.orc_gmm_fwd.restype = I64
             L.orc_dequantize.argtypes = [P, P, I32, I64, I64, P]
             L.orc_gmm_dlhs.argtypes = [P, I64, I64, P, P, I32, I64, P, P, I64, P, P]
+            L.orc_dswiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
+            L.orc_dswiglu.restype = None
             L.orc_gmm_dlhs.restype = I64
             L.orc_tgmm_quantize_tiles.argtypes = [P, P, I64, I64, I64, I32, P, I64,
                                                   P, P, P, P, P]
@@ -162,6 +164,34 @@ def gmm_dlhs(dout, codes, scale, gs, rows=None, fill=None, want_f64=False):
                              _p(scale.contiguous()), E, K, _p(gs), _p(r),
                              0 if r is None else r.numel(), _p(out), _p(out64))
     return out.view(torch.bfloat16), out64, bad
+
+
+def dswiglu(dh_f64, gu, rows=None, fill=None, want_f64=False):
+    """SwiGLU backward: dgu bf16 [M, 2F] from the unrounded upstream gradient
+    dh (float64 [M, F]) and the wi output gu (bf16 [M, 2F], gate | up)."""
+    M, F = dh_f64.shape
+    assert gu.shape == (M, 2 * F)
+    out = torch.full((M, 2 * F), 0 if fill is None else fill, dtype=torch.int16)
+    out64 = torch.full((M, 2 * F), float("nan"), dtype=torch.float64) if want_f64 else None
+    r = None if rows is None else rows.to(torch.int64).contiguous()
+    lib().orc_dswiglu(_p(dh_f64.contiguous()), _p(gu.contiguous()), M, F, _p(r),
+                      0 if r is None else r.numel(), _p(out), _p(out64))
+    return out.view(torch.bfloat16), out64
+
+
+def gmm_dlhs_dswiglu(dout, codes, scale, gu, gs, rows=None, fill=None, want_f64=False):
+    """wo dLHS followed by the SwiGLU backward: dgu bf16 [M, 2F] where
+    dh = dout [M, N] x dequant(codes)[e]^T ([E, F, N] codes) is kept unrounded."""
+    M, N = dout.shape
+    E, F, N2 = codes.shape
+    assert N2 == N and gu.shape == (M, 2 * F)
+    _, dh64, bad = gmm_dlhs(dout, codes, scale, gs, rows=rows, want_f64=True)
+    dh64 = torch.nan_to_num(dh64, nan=0.0)      # rows the dLHS did not compute
+    if rows is None:
+        T = int(_gs(gs).clamp_min(0).sum().clamp_max(M))
+        rows = torch.arange(T, dtype=torch.int64)
+    out, out64 = dswiglu(dh64, gu, rows=rows, fill=fill, want_f64=want_f64)
+    return out, out64, bad
 
 
 def segment_bound(M: int, E: int) -> int:

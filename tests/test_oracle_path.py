@@ -8,6 +8,9 @@
   case that reduces to the plain matmul, zero-size groups write nothing, locality;
 * dequantization: bit-identical to torch's codes x scale -> bf16;
 * dLHS: float64 torch matmul per group with the dequantized weights;
+* dSwiGLU (the SwiGLU backward fused into the wo dLHS): torch autograd of
+  silu(g) * u in float64, exact special values, and the fused op equal to a
+  per-group float64 matmul followed by autograd;
 * tgmm: a lossless special case equal to X_e^T D_e (textbook), brute force in
   plain Python on a tiny case, tail invariance, locality, empty experts.
 
@@ -223,6 +226,61 @@ def test_dlhs_matches_float64_matmul_per_group(orc):
         if b > a:
             ref = d[a:b].double() @ wb[e].T
             assert torch.allclose(out64[a:b], ref, rtol=1e-12, atol=1e-300)
+    assert (out.view(torch.int16)[80:] == 0x7BCD).all()
+
+
+# ------------------------------------------------------ dSwiGLU (wo backward)
+def _autograd_dswiglu(dh64, gu):
+    """Gradients of sum(dh * silu(g) * u) w.r.t. g and u, float64 autograd."""
+    F = dh64.shape[1]
+    g = gu[:, :F].double().clone().requires_grad_(True)
+    u = gu[:, F:].double().clone().requires_grad_(True)
+    (torch.nn.functional.silu(g) * u).backward(dh64)
+    return g.grad, u.grad
+
+
+def test_dswiglu_matches_float64_autograd(orc):
+    M, F = 40, 24
+    gen = torch.Generator().manual_seed(3)
+    dh = torch.randn(M, F, generator=gen, dtype=torch.float64) * 3
+    gu = (torch.randn(M, 2 * F, generator=gen) * 4).to(torch.bfloat16)
+    out, out64 = orc.dswiglu(dh, gu, want_f64=True)
+    dg, du = _autograd_dswiglu(dh, gu)
+    assert torch.allclose(out64[:, :F], dg, rtol=1e-12, atol=1e-300)
+    assert torch.allclose(out64[:, F:], du, rtol=1e-12, atol=1e-300)
+    # one rounding to bf16 of the exact value
+    assert torch.equal(out.view(torch.int16), orc.f64_to_bf16(out64).view(torch.int16))
+
+
+def test_dswiglu_special_values(orc):
+    # g = 0: silu(0) = 0 and silu'(0) = 1/2 -> du = 0, dg = dh * u / 2 (exact)
+    # large |g|: sig -> 1 (silu' -> 1, silu -> g) or sig -> 0 (both -> 0)
+    F = 4
+    gu = torch.tensor([[0.0, 0.0, 60.0, -80.0, 2.0, -3.0, 1.5, 0.25]], dtype=torch.bfloat16)
+    dh = torch.tensor([[1.5, -0.75, 2.0, 5.0]], dtype=torch.float64)
+    _, out64 = orc.dswiglu(dh, gu, want_f64=True)
+    assert out64[0, 0].item() == 1.5 * 2.0 / 2 and out64[0, 1].item() == -0.75 * -3.0 / 2
+    assert out64[0, F + 0].item() == 0.0 and out64[0, F + 1].item() == 0.0
+    assert abs(out64[0, 2].item() - 2.0 * 1.5) < 1e-20          # silu'(60) = 1 - O(60 e^-60)
+    assert abs(out64[0, F + 2].item() - 2.0 * 60.0) < 1e-20
+    assert abs(out64[0, 3].item()) < 1e-30 and abs(out64[0, F + 3].item()) < 1e-30
+
+
+def test_gmm_dlhs_dswiglu_is_matmul_then_autograd(orc):
+    M, N, F, E = 90, 64, 40, 3
+    gs = torch.tensor([25, 0, 55], dtype=torch.int32)
+    d = W.fill_tail_garbage(W.cotangent(M, N, 13), 80)
+    gu = W.fill_tail_garbage(W.activations(M, 2 * F, 14), 80)
+    codes, scale = W.fp8_weights(E, F, N, 0.05, 15)
+    out, out64, bad = orc.gmm_dlhs_dswiglu(d, codes, scale, gu, gs, want_f64=True, fill=0x7BCD)
+    assert bad == 0
+    wb = (codes.view(F8).float() * scale[:, None, :]).to(torch.bfloat16).double()
+    for e, (a, b) in enumerate([(0, 25), (25, 25), (25, 80)]):
+        if b > a:
+            dh = d[a:b].double() @ wb[e].T
+            dg, du = _autograd_dswiglu(dh, gu[a:b])
+            assert torch.allclose(out64[a:b, :F], dg, rtol=1e-9, atol=1e-12)
+            assert torch.allclose(out64[a:b, F:], du, rtol=1e-9, atol=1e-12)
     assert (out.view(torch.int16)[80:] == 0x7BCD).all()
 
 
