@@ -442,6 +442,16 @@ def main():
                                   "gbs": round(deq_bytes / (t_deq * 1e-3) / 1e9, 1),
                                   "frac_of_hbm": round(deq_bytes / (t_deq * 1e-3) / 1e9 / pk["hbm"], 3)}
         del w_bf, wo_bf
+        # wo dLHS with the SwiGLU backward fused (gu: any [M, 2F] bf16 tensor of
+        # the wi output's shape; the cotangent buffer stands in for it)
+        dgu_out = torch.empty(M, 2 * FF, dtype=torch.bfloat16, device=inp["dgu"].device)
+        t_dsw = timeit(lambda: fb.gmm_dlhs_dswiglu_fp8(inp["dy"], inp["wo_c"], inp["wo_s"], inp["dgu"],
+                                                       inp["gs"], out=dgu_out))
+        extra["wo_dlhs_dswiglu"] = {
+            "ms": round(t_dsw, 4), "wo_dlhs_ms": round(per["wo_dlhs"], 4),
+            "tflops": round(flops["wo_dlhs"] / (t_dsw * 1e-3) / 1e12, 1),
+            "extra_bytes": "reads gu [M, 2F], writes dgu [M, 2F] instead of dh [M, F]"}
+        del dgu_out
         extra["microbench"] = microbench(fb, timeit, torch.device("cuda", torch.cuda.current_device()))
 
     # ------------------------------------------------------------------ e2e

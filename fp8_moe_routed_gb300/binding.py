@@ -39,6 +39,7 @@ EXPORTS = [
     "fp8moe_dequantize_fp8_codes", "fp8moe_gmm_bf16_fwd", "fp8moe_quantize_rows",
     "fp8moe_tgmm_quantize_tiles", "fp8moe_read_status", "fp8moe_status_string",
     "fp8moe_last_cuda_error", "fp8moe_num_sms", "fp8moe_gmm_silu_fp8_fwd_noalloc",
+    "fp8moe_gmm_dlhs_dswiglu_fp8", "fp8moe_gmm_dlhs_dswiglu_fp8_path",
 ]
 
 _lock = threading.Lock()
@@ -82,6 +83,9 @@ def load(build_if_missing: bool = True):
             "fp8moe_last_cuda_error": ([], I32),
             "fp8moe_num_sms": ([], I32),
             "fp8moe_gmm_silu_fp8_fwd_noalloc": ([P, I64, I64, P, P, I32, I64, P, P, P], I32),
+            "fp8moe_gmm_dlhs_dswiglu_fp8": ([P, I64, I64, P, P, I32, I64, P, P, P, P, SZ, P], I32),
+            "fp8moe_gmm_dlhs_dswiglu_fp8_path": ([P, I64, I64, P, P, I32, I64, P, P, P, I32, P],
+                                                 I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -215,6 +219,37 @@ def gmm_dlhs_fp8(dout, codes, scale, group_sizes, out=None, path: Optional[int] 
         rc = L.fp8moe_gmm_dlhs_fp8_path(_ptr(dout), M, N, _ptr(codes), _ptr(scale), E, K,
                                         _ptr(group_sizes), _ptr(out), int(path), st)
     _check(rc, "fp8moe_gmm_dlhs_fp8")
+    return out
+
+
+def gmm_dlhs_dswiglu_fp8(dout, codes, scale, gu, group_sizes, out=None,
+                         path: Optional[int] = None):
+    """wo dLHS + SwiGLU backward: dgu bf16 [M, 2F] from dout [M, N], the wo
+    codes [E, F, N] and the wi output gu [M, 2F] (see fp8moe_gmm_dlhs_dswiglu_fp8;
+    path forces 0 streaming / 1 cached)."""
+    L = load()
+    _req(dout, torch.bfloat16, "dout", 2)
+    _req(codes, torch.uint8, "codes", 3)
+    _req(scale, torch.float32, "scale", 2)
+    _req(gu, torch.bfloat16, "gu", 2)
+    _req(group_sizes, torch.int32, "group_sizes", 1)
+    M, N = dout.shape
+    E, F, N2 = codes.shape
+    if N2 != N or scale.shape != (E, N) or group_sizes.numel() != E or gu.shape != (M, 2 * F):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty(M, 2 * F, dtype=torch.bfloat16, device=dout.device)
+    else:
+        _req(out, torch.bfloat16, "out", 2)
+    st = _stream(dout.device)
+    if path is None:
+        rc = L.fp8moe_gmm_dlhs_dswiglu_fp8(_ptr(dout), M, N, _ptr(codes), _ptr(scale), E, F,
+                                           _ptr(gu), _ptr(group_sizes), _ptr(out), None, 0, st)
+    else:
+        rc = L.fp8moe_gmm_dlhs_dswiglu_fp8_path(_ptr(dout), M, N, _ptr(codes), _ptr(scale), E,
+                                                F, _ptr(gu), _ptr(group_sizes), _ptr(out),
+                                                int(path), st)
+    _check(rc, "fp8moe_gmm_dlhs_dswiglu_fp8")
     return out
 
 

@@ -188,20 +188,23 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   return FP8MOE_OK;
 }
 
+// gu != nullptr selects the dSwiGLU epilogue: dlhs is then dgu [M, 2K].
 int dlhs_impl(const void* dout, int64_t M, int64_t N, const uint8_t* codes, const float* scale,
-              int32_t E, int64_t K, const int32_t* gs, void* dlhs, int path, cudaStream_t stream) {
+              int32_t E, int64_t K, const int32_t* gs, const void* gu, void* dlhs, int path,
+              cudaStream_t stream) {
   int rc = check_common(M, K, N, E);
   if (rc) return rc;
   if (path == 1 && N > 256) return FP8MOE_EINVAL;
   if (M == 0) return FP8MOE_OK;
   if (!dout || !codes || !scale || !gs || !dlhs) return FP8MOE_EINVAL;
   if (!aligned16(dout) || !aligned16(codes) || !aligned16(scale) || !aligned16(dlhs) ||
-      (reinterpret_cast<uintptr_t>(gs) & 3u))
+      (gu && !aligned16(gu)) || (reinterpret_cast<uintptr_t>(gs) & 3u))
     return FP8MOE_EALIGN;
   int sms = 0;
   rc = device_init(&sms);
   if (rc) return rc;
   GmmDlhsArgs a;
+  a.gu = gu;
   {
     const uint64_t dims[2] = {(uint64_t)N, (uint64_t)M};
     const uint64_t st[1] = {(uint64_t)N * 2};
@@ -281,7 +284,7 @@ int fp8moe_gmm_dlhs_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* c
   (void)workspace_bytes;
   // the on-chip cache path when the whole contraction fits one cached block
   const int path = (N <= 256) ? 1 : 0;
-  return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, dlhs, path, stream);
+  return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, nullptr, dlhs, path, stream);
 }
 
 int fp8moe_gmm_dlhs_fp8_path(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
@@ -289,7 +292,27 @@ int fp8moe_gmm_dlhs_fp8_path(const void* dout, int64_t M, int64_t N, const uint8
                              const int32_t* group_sizes, void* dlhs, int32_t path,
                              fp8moe_stream_t stream) {
   if (path != 0 && path != 1) return FP8MOE_EINVAL;
-  return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, dlhs, path, stream);
+  return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, nullptr, dlhs, path, stream);
+}
+
+int fp8moe_gmm_dlhs_dswiglu_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
+                                const float* scale, int32_t E, int64_t F, const void* gu,
+                                const int32_t* group_sizes, void* dgu, void* workspace,
+                                size_t workspace_bytes, fp8moe_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (M > 0 && !gu) return FP8MOE_EINVAL;
+  const int path = (N <= 256) ? 1 : 0;
+  return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
+}
+
+int fp8moe_gmm_dlhs_dswiglu_fp8_path(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
+                                     const float* scale, int32_t E, int64_t F, const void* gu,
+                                     const int32_t* group_sizes, void* dgu, int32_t path,
+                                     fp8moe_stream_t stream) {
+  if (path != 0 && path != 1) return FP8MOE_EINVAL;
+  if (M > 0 && !gu) return FP8MOE_EINVAL;
+  return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
 }
 
 int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,

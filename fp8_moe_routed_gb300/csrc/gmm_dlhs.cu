@@ -24,6 +24,11 @@
 //   warps 2..5   epilogue: TMEM -> bf16 -> row-masked stores. TMEM holds two
 //                accumulators: the two m tiles of a streaming unit, or (cached)
 //                consecutive m tiles so that the epilogue overlaps the MMAs.
+// dSwiGLU variant (DSW): the wo dLHS of "gmm_dswiglu_fp8" ([NQ] Implementation)
+// with the SwiGLU backward in the epilogue. The accumulator is dh = dL/dh for
+// h = silu(g) * u; the epilogue reads g and u from the wi output gu [M, 2F] and
+// writes dgu [M, 2F]: dg = dh * u * sig(g) * (1 + g * (1 - sig(g))) in columns
+// [0, F) and du = dh * g * sig(g) in [F, 2F), so dh itself never reaches HBM.
 // Cached variant (the contraction fits in <= 4 steps, i.e. N <= 256): a work
 // unit is (expert, k tile, run of m tiles); the whole dequantized
 // [256 x N] block stays in shared memory and only dout tiles stream. Both
@@ -189,11 +194,74 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int r, bool row_ok,
   }
 }
 
-template <bool CACHED>
+// dSwiGLU epilogue of one finished accumulator (dh, 128 rows x 256 columns of
+// F): g = gurow[f], u = gurow[F + f] -> dgu row: dg at f, du at F + f.
+__device__ __forceinline__ void dswiglu8(const uint4& gw, const uint4& uw, const uint32_t* v,
+                                         uint32_t* og, uint32_t* ou) {
+  const uint32_t gg[4] = {gw.x, gw.y, gw.z, gw.w};
+  const uint32_t uu[4] = {uw.x, uw.y, uw.z, uw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float dg[2], du[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float g = __uint_as_float((gg[i] >> (16 * h)) << 16);
+      const float u = __uint_as_float((uu[i] >> (16 * h)) << 16);
+      const float d = __uint_as_float(v[2 * i + h]);
+      const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+      const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
+      dg[h] = __fmul_rn(__fmul_rn(d, u), dsilu);
+      du[h] = __fmul_rn(d, __fmul_rn(g, sg));
+    }
+    og[i] = f32x2_to_bf16x2(dg[0], dg[1]);
+    ou[i] = f32x2_to_bf16x2(du[0], du[1]);
+  }
+}
+
+__device__ __forceinline__ void store_tile_dswiglu(uint32_t tbase, bool row_ok,
+                                                   const __nv_bfloat16* __restrict__ gurow,
+                                                   __nv_bfloat16* __restrict__ orow, int col_base,
+                                                   int F) {
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tbase + c * 32, v);
+    tmem_ld_wait();
+    const int col0 = col_base + c * 32;
+    if (!row_ok || col0 >= F) continue;
+    if (col0 + 32 <= F) {
+      const uint4* gp = reinterpret_cast<const uint4*>(gurow + col0);
+      const uint4* up = reinterpret_cast<const uint4*>(gurow + F + col0);
+      uint4* dgp = reinterpret_cast<uint4*>(orow + col0);
+      uint4* dup = reinterpret_cast<uint4*>(orow + F + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t og[4], ou[4];
+        dswiglu8(__ldg(gp + q), __ldg(up + q), v + 8 * q, og, ou);
+        dgp[q] = make_uint4(og[0], og[1], og[2], og[3]);
+        dup[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+      }
+    } else {
+      // F % 16 == 0: the valid part of this chunk is whole 8-column groups
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (col0 + 8 * q >= F) break;
+        uint32_t og[4], ou[4];
+        dswiglu8(__ldg(reinterpret_cast<const uint4*>(gurow + col0 + 8 * q)),
+                 __ldg(reinterpret_cast<const uint4*>(gurow + F + col0 + 8 * q)), v + 8 * q, og, ou);
+        *reinterpret_cast<uint4*>(orow + col0 + 8 * q) = make_uint4(og[0], og[1], og[2], og[3]);
+        *reinterpret_cast<uint4*>(orow + F + col0 + 8 * q) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+      }
+    }
+  }
+}
+
+template <bool CACHED, bool DSW>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                 const float* __restrict__ scale, const int32_t* __restrict__ gs,
-                __nv_bfloat16* __restrict__ dlhs, int64_t M, int N, int K, int E) {
+                const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ dlhs, int64_t M,
+                int N, int K, int E) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -413,7 +481,10 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           col_acc = acc;
         }
         const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(col_acc * kBN);
-        store_tile(tbase, r, row_ok, dlhs + row * K, t.j * kBN, K);
+        if (DSW)
+          store_tile_dswiglu(tbase, row_ok, gu + row * 2 * K, dlhs + row * 2 * K, t.j * kBN, K);
+        else
+          store_tile(tbase, r, row_ok, dlhs + row * K, t.j * kBN, K);
         if (CACHED) {
           tc_fence_before();
           __syncwarp();
@@ -486,13 +557,14 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
-template <bool CACHED>
+template <bool CACHED, bool DSW>
 cudaError_t launch(const GmmDlhsArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gmm_dlhs_kernel<CACHED>;
+  auto kern = gmm_dlhs_kernel<CACHED, DSW>;
   constexpr size_t bytes = smem_bytes<CACHED>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (err != cudaSuccess) return err;
   kern<<<num_sms, kThreads, bytes, s>>>(a.tmA, a.tmC, a.scale, a.gs,
+                                        static_cast<const __nv_bfloat16*>(a.gu),
                                         static_cast<__nv_bfloat16*>(a.dlhs), a.M, a.N, a.K, a.E);
   return cudaGetLastError();
 }
@@ -503,5 +575,8 @@ cudaError_t launch(const GmmDlhsArgs& a, int num_sms, cudaStream_t s) {
 FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_dlhs)
 
 cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int cached, cudaStream_t s) {
-  return cached ? fp8moe::dlhs::launch<true>(a, num_sms, s) : fp8moe::dlhs::launch<false>(a, num_sms, s);
+  using namespace fp8moe::dlhs;
+  if (a.gu)
+    return cached ? launch<true, true>(a, num_sms, s) : launch<false, true>(a, num_sms, s);
+  return cached ? launch<true, false>(a, num_sms, s) : launch<false, false>(a, num_sms, s);
 }

@@ -35,7 +35,8 @@ struct GmmDlhsArgs {
   CUtensorMap tmC;        // codes [E, K, N] u8 tiles
   const float* scale;     // [E, N]
   const int32_t* gs;
-  void* dlhs;             // bf16 [M, K]
+  const void* gu;         // bf16 [M, 2K] wi output (gate | up) for the dSwiGLU epilogue, or null
+  void* dlhs;             // bf16 [M, K], or [M, 2K] dgu with the dSwiGLU epilogue
   int64_t M;
   int N, K, E;
 };

@@ -120,6 +120,29 @@ int fp8moe_gmm_dlhs_fp8_path(const void* dout, int64_t M, int64_t N, const uint8
                              const int32_t* group_sizes, void* dlhs, int32_t path,
                              fp8moe_stream_t stream);
 
+/* wo dLHS with the SwiGLU backward fused into its epilogue -- [NQ]
+ * Implementation (gmm_dswiglu_fp8, the wo op whose backward also undoes the wi
+ * SwiGLU).  With codes/scale the wo weight [E, F, N] / [E, N]:
+ *   dh[m,f]  = sum_n dout[m,n] * w[e,f,n]   (as fp8moe_gmm_dlhs_fp8, f32, not rounded)
+ *   g = gu[m,f], u = gu[m,F+f], sig(z) = 1 / (1 + exp(-z))
+ *   dgu[m,f]   = bf16( dh * u * sig(g) * (1 + g * (1 - sig(g))) )     (dg)
+ *   dgu[m,F+f] = bf16( dh * g * sig(g) )                              (du)
+ * gu: bf16 [M, 2F], the wi forward output before SwiGLU (gate | up halves).
+ * dgu: bf16 [M, 2F]; rows >= T untouched; dh is never written to memory.
+ * Pointers 16-byte aligned; F % 16 == 0 and N % 16 == 0 (FP8MOE_EALIGN);
+ * gu NULL with M > 0: FP8MOE_EINVAL.  No workspace (pass NULL, 0). */
+int fp8moe_gmm_dlhs_dswiglu_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
+                                const float* scale, int32_t E, int64_t F, const void* gu,
+                                const int32_t* group_sizes, void* dgu, void* workspace,
+                                size_t workspace_bytes, fp8moe_stream_t stream);
+
+/* fp8moe_gmm_dlhs_dswiglu_fp8 with the internal path forced (0 streaming,
+ * 1 on-chip weight cache, N <= 256); both give identical bits. */
+int fp8moe_gmm_dlhs_dswiglu_fp8_path(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
+                                     const float* scale, int32_t E, int64_t F, const void* gu,
+                                     const int32_t* group_sizes, void* dgu, int32_t path,
+                                     fp8moe_stream_t stream);
+
 /* Weight-gradient tgmm with in-kernel per-tile operand quantization -- [DQ]
  * What.  Segments: the global 128-row tiles [128t, 128t+128) intersected with
  * each group.  Per segment q and channel:

@@ -207,3 +207,23 @@ def test_microbench_shape_forward_and_dlhs_sampled(orc):
     ref_dx, _, bad = orc.gmm_dlhs(dgu.cpu(), wi_cc, wi_sc, gs, rows=rows_b)
     assert bad == 0
     check_bf16(dx.cpu()[rows_b], ref_dx[rows_b], what="microbench wi dlhs")
+
+
+def test_balanced_wo_dlhs_dswiglu_sampled(orc):
+    """wo dLHS with the SwiGLU backward fused (balanced layer): gu is the wi
+    forward output before SwiGLU, dout ~ N(0, 1); sampled rows vs the oracle."""
+    E, K, F, M = 32, 7168, 2048, 32768
+    gs = W.group_sizes("balanced", E=E, M=M)
+    gsd = gs.to(DEV)
+    x = W.activations(M, K, 61, outlier_frac=0.001, device=DEV)
+    wi_c, wi_s = W.fp8_weights(E, K, 2 * F, 0.006, 62, device=DEV)
+    wo_c, wo_s = W.fp8_weights(E, F, K, 0.006, 63, device=DEV)
+    gu = fb.gmm_fp8_fwd(x, wi_c, wi_s, gsd)             # [M, 2F], gate | up
+    del x, wi_c
+    dy = W.cotangent(M, K, 64, device=DEV)
+    dgu = fb.gmm_dlhs_dswiglu_fp8(dy, wo_c, wo_s, gu, gsd)
+    assert torch.isfinite(dgu.float()).all()
+    rows = sample_rows(gs, 1, seed=11)[::2]
+    ref, _, bad = orc.gmm_dlhs_dswiglu(dy.cpu(), wo_c.cpu(), wo_s.cpu(), gu.cpu(), gs, rows=rows)
+    assert bad == 0
+    check_bf16(dgu.cpu()[rows], ref[rows], what="balanced wo dlhs+dswiglu")

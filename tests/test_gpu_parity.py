@@ -163,6 +163,57 @@ def test_dlhs_vs_oracle_and_paths_identical(orc, M, N, K, E, gs):
         assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
 
 
+# ---------------------------------------------------- wo dLHS + dSwiGLU
+DSWIGLU_CASES = [
+    (512, 256, 128, 4, "tiny"),                       # N <= 256: both paths
+    (1024, 512, 272, 3, [300, 0, 500]),               # F = 272: partial column chunk
+    (640, 160, 64, 2, [0, 600]),                      # first expert empty, both paths
+]
+
+
+@pytest.mark.parametrize("M,N,F,E,gs", DSWIGLU_CASES)
+def test_dlhs_dswiglu_vs_oracle_and_paths_identical(orc, M, N, F, E, gs):
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=5, M=M, E=E)
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    T = int(gs.sum())
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=N + 1), T)
+    gu = W.fill_tail_garbage(W.activations(M, 2 * F, seed=F + 2), T)
+    codes, scale = W.fp8_weights(E, F, N, 0.05, seed=E + 3)
+    dg, gug, cg, sg, gsg = cuda(d, gu, codes, scale, gs)
+    out0 = torch.full((M, 2 * F), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg, out=out0, path=0)
+    ref, _, bad = orc.gmm_dlhs_dswiglu(d, codes, scale, gu, gs)
+    assert bad == 0
+    check_bf16(out0[:T], ref[:T], what="dlhs+dswiglu streaming")
+    assert (out0[T:] == 7.0).all(), "rows >= T were written"
+    if N <= 256:
+        out1 = torch.full((M, 2 * F), 7.0, dtype=torch.bfloat16, device=DEV)
+        fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg, out=out1, path=1)
+        assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
+    # the default entry point picks one of the two paths
+    out2 = fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg)
+    assert torch.equal(bits16(out2[:T]), bits16(out0[:T]))
+
+
+def test_dlhs_dswiglu_rejects_missing_gu_and_misalignment():
+    M, N, F, E = 128, 256, 64, 2
+    gs = torch.tensor([64, 64], dtype=torch.int32, device=DEV)
+    d = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros(E, F, N, dtype=torch.uint8, device=DEV)
+    scale = torch.ones(E, N, dtype=torch.float32, device=DEV)
+    out = torch.empty(M, 2 * F, dtype=torch.bfloat16, device=DEV)
+    L = fb.load()
+    st = fb._stream(d.device)
+    rc = L.fp8moe_gmm_dlhs_dswiglu_fp8(fb._ptr(d), M, N, fb._ptr(codes), fb._ptr(scale), E, F,
+                                       None, fb._ptr(gs), fb._ptr(out), None, 0, st)
+    assert rc == -1
+    gu = torch.zeros(M * 2 * F + 8, dtype=torch.bfloat16, device=DEV)[1:1 + M * 2 * F]
+    rc = L.fp8moe_gmm_dlhs_dswiglu_fp8(fb._ptr(d), M, N, fb._ptr(codes), fb._ptr(scale), E, F,
+                                       fb._ptr(gu), fb._ptr(gs), fb._ptr(out), None, 0, st)
+    assert rc == -2
+
+
 # ------------------------------------------------------------------- tgmm
 TGMM_CASES = [
     (512, 256, 256, 4, "tiny"),
