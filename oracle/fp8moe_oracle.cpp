@@ -14,6 +14,8 @@
 //          gradient dtype" -- section What.
 //   [SM]  "Fix fp8 MoE on the sparse_matmul path" -- section Fix (names the
 //          forward dtype float8_e4m3fn).
+//   [DQ] What also makes the gradient fp8 dtype configurable, e5m2 (the
+//   recipe's default) or e4m3: here the tgmm's dout operand may be e5m2.
 //   The SwiGLU backward (dSwiGLU) is the derivative of silu(g) * u written out;
 //   [NQ] Implementation names the op that fuses it into the wo GMM
 //   (gmm_dswiglu_fp8).
@@ -21,7 +23,9 @@
 // Floating point: all sums are taken in double. Products of two e4m3 values are
 // multiples of 2^-18 with magnitude <= 448^2, so any sum of up to 2^17 of them is
 // exact in double whatever the order; the forward GMM accumulator is therefore the
-// exact value, rounded once at the end. Quantization decisions (scales, codes) are
+// exact value, rounded once at the end. With an e5m2 operand (tgmm, multiples of
+// 2^-16 up to 57344) a 128-term segment dot product can need more than 53 bits;
+// it is then within 128 * 2^-53 relative of the exact value. Quantization decisions (scales, codes) are
 // taken in f32, the precision the pages fix for the activation scale.
 //
 // Data-dependent bounds: group sizes are clamped like the library documents
@@ -138,6 +142,62 @@ uint8_t e4m3_encode(float f) {
 }
 
 // ---------------------------------------------------------------------------
+// OCP float8 e5m2 ([DQ] What: the gradient fp8 dtype, e5m2 by default).
+// Layout s.eeeee.mm, exponent bias 15, exponent field 0 holds subnormals
+// m * 2^-16, exponent field 31 holds +-Inf (m = 0) and NaN (m != 0); largest
+// finite value 1.75 * 2^15 = 57344.
+// ---------------------------------------------------------------------------
+double e5m2_decode(uint8_t c) {
+  int s = (c >> 7) & 1;
+  int e = (c >> 2) & 0x1F;
+  int m = c & 0x3;
+  double v;
+  if (e == 0x1F) v = m == 0 ? HUGE_VAL : std::nan("");
+  else if (e == 0) v = std::ldexp((double)m, -16);
+  else v = std::ldexp(1.0 + m / 4.0, e - 15);
+  return s ? -v : v;
+}
+
+// The 124 non-negative finite values, code 0x00 .. 0x7B, ascending.
+struct E5m2Table {
+  double v[124];
+  E5m2Table() { for (int c = 0; c < 124; ++c) v[c] = e5m2_decode((uint8_t)c); }
+};
+const E5m2Table& e5m2_table() { static E5m2Table t; return t; }
+
+// Round an f32 to e5m2: nearest value, ties to the even code; magnitudes past
+// the largest finite value (including infinities) saturate to +-57344 (the
+// finite-saturating conversion: a scaled operand never becomes infinite);
+// NaN -> 0x7F.
+uint8_t e5m2_encode(float f) {
+  if (std::isnan(f)) return 0x7F;
+  uint8_t sign = std::signbit(f) ? 0x80 : 0x00;
+  double a = std::fabs((double)f);
+  const double* v = e5m2_table().v;
+  if (a >= v[123]) return sign | 123;
+  int lo = 0, hi = 123;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (v[mid] <= a) lo = mid; else hi = mid;
+  }
+  int c = lo;
+  double d_lo = a - v[c], d_hi = v[c + 1] - a;
+  int pick;
+  if (d_lo < d_hi) pick = c;
+  else if (d_hi < d_lo) pick = c + 1;
+  else pick = (c % 2 == 0) ? c : c + 1;
+  return sign | (uint8_t)pick;
+}
+
+// An fp8 format of the tgmm's dout operand: 0 = e4m3fn, 1 = e5m2.
+struct Fp8Fmt {
+  int32_t id;
+  float max() const { return id == 1 ? 57344.0f : 448.0f; }
+  uint8_t encode(float f) const { return id == 1 ? e5m2_encode(f) : e4m3_encode(f); }
+  double decode(uint8_t c) const { return id == 1 ? e5m2_decode(c) : e4m3_decode(c); }
+};
+
+// ---------------------------------------------------------------------------
 // Ragged groups.  Rows of expert e are [off[e], off[e] + gs[e]), off = exclusive
 // prefix sum, in the static buffer of M rows ([DQ] What: the buffer has a static
 // size; only rows covered by group_sizes are valid).  Clamping: negative sizes
@@ -189,6 +249,12 @@ extern "C" {
 
 // ----- codec access for the pin tests -------------------------------------
 double orc_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+double orc_e5m2_decode(uint8_t c) { return e5m2_decode(c); }
+
+void orc_e5m2_encode_f32(const float* x, int64_t n, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = e5m2_encode(x[i]);
+}
 
 void orc_e4m3_encode_f32(const float* x, int64_t n, uint8_t* out) {
 #pragma omp parallel for schedule(static)
@@ -394,6 +460,9 @@ void orc_dswiglu(const double* dh, const uint16_t* gu, int64_t M, int64_t F,
 // of the buffer, intersected with each group (a tile shared by two groups is
 // two segments with their own scales).  Per segment and column:
 // s = max(amax over the segment's rows, 1e-12) / 448 in f32, codes = e4m3(x / s).
+// With d_fmt = 1 the dout operand is e5m2 instead ([DQ] What, the gradient
+// dtype): s = max(amax, 1e-12) / 57344 (reading: the same rule with the e5m2
+// maximum), codes = e5m2(x / s).
 //
 // Segments are numbered expert by expert, tiles ascending, empty experts have
 // none.  Output layout (the library's debug export uses the same): for segment
@@ -405,7 +474,7 @@ int64_t orc_tgmm_quantize_tiles(const uint16_t* lhs, const uint16_t* dout,
                                 int64_t M, int64_t K, int64_t N, int32_t E,
                                 const int32_t* gs, int64_t Smax,
                                 uint8_t* qx, float* sx, uint8_t* qd, float* sd,
-                                int64_t* nseg) {
+                                int64_t* nseg, int32_t d_fmt) {
   Groups g(gs, E, M);
   std::atomic<int64_t> bad{0};
   RowGuard guard{g.T, &bad};
@@ -431,6 +500,7 @@ int64_t orc_tgmm_quantize_tiles(const uint16_t* lhs, const uint16_t* dout,
       int64_t C = pass == 0 ? K : N;
       uint8_t* qo = (pass == 0 ? qx : qd) + q * 128 * C;
       float* so = (pass == 0 ? sx : sd) + q * C;
+      const Fp8Fmt fmt{pass == 0 ? 0 : d_fmt};
       std::memset(qo, 0, (size_t)(128 * C));
       for (int64_t c = 0; c < C; ++c) {
         float amax = 0.0f;
@@ -438,11 +508,11 @@ int64_t orc_tgmm_quantize_tiles(const uint16_t* lhs, const uint16_t* dout,
           if (!guard.ok(m)) continue;
           amax = std::max(amax, std::fabs(bf16_to_f32(src[m * C + c])));
         }
-        float s = std::max(amax, kEps) / kE4m3Max;
+        float s = std::max(amax, kEps) / fmt.max();
         so[c] = s;
         for (int64_t m = r0; m < r1; ++m) {
           if (!guard.ok(m)) continue;
-          qo[(m - t * 128) * C + c] = e4m3_encode(bf16_to_f32(src[m * C + c]) / s);
+          qo[(m - t * 128) * C + c] = fmt.encode(bf16_to_f32(src[m * C + c]) / s);
         }
       }
     }
@@ -460,7 +530,7 @@ int64_t orc_tgmm_quantize_tiles(const uint16_t* lhs, const uint16_t* dout,
 int64_t orc_tgmm(const uint16_t* lhs, const uint16_t* dout, int64_t M, int64_t K,
                  int64_t N, int32_t E, const int32_t* gs,
                  const int32_t* experts, int32_t nexperts,
-                 int64_t k0, int64_t k1, int64_t n0, int64_t n1, float* dW) {
+                 int64_t k0, int64_t k1, int64_t n0, int64_t n1, float* dW, int32_t d_fmt) {
   Groups g(gs, E, M);
   std::atomic<int64_t> bad{0};
   RowGuard guard{g.T, &bad};
@@ -483,6 +553,7 @@ int64_t orc_tgmm(const uint16_t* lhs, const uint16_t* dout, int64_t M, int64_t K
           int64_t c0 = pass == 0 ? k0 : n0, CB = pass == 0 ? KB : NB;
           std::vector<float>& s_out = pass == 0 ? sxs : sds;
           std::vector<double>& q_out = pass == 0 ? qxv : qdv;
+          const Fp8Fmt fmt{pass == 0 ? 0 : d_fmt};
 #pragma omp parallel for schedule(static)
           for (int64_t c = 0; c < CB; ++c) {
             float amax = 0.0f;
@@ -490,11 +561,11 @@ int64_t orc_tgmm(const uint16_t* lhs, const uint16_t* dout, int64_t M, int64_t K
               if (!guard.ok(m)) continue;
               amax = std::max(amax, std::fabs(bf16_to_f32(src[m * C + c0 + c])));
             }
-            float s = std::max(amax, kEps) / kE4m3Max;
+            float s = std::max(amax, kEps) / fmt.max();
             s_out[c] = s;
             for (int64_t m = r0; m < r1; ++m) {
               if (!guard.ok(m)) continue;
-              q_out[(m - r0) * CB + c] = e4m3_decode(e4m3_encode(bf16_to_f32(src[m * C + c0 + c]) / s));
+              q_out[(m - r0) * CB + c] = fmt.decode(fmt.encode(bf16_to_f32(src[m * C + c0 + c]) / s));
             }
           }
         }

@@ -61,10 +61,14 @@ def lib():
             L.orc_dswiglu.restype = None
             L.orc_gmm_dlhs.restype = I64
             L.orc_tgmm_quantize_tiles.argtypes = [P, P, I64, I64, I64, I32, P, I64,
-                                                  P, P, P, P, P]
+                                                  P, P, P, P, P, I32]
             L.orc_tgmm_quantize_tiles.restype = I64
             L.orc_tgmm.argtypes = [P, P, I64, I64, I64, I32, P, P, I32,
-                                   I64, I64, I64, I64, P]
+                                   I64, I64, I64, I64, P, I32]
+            L.orc_e5m2_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e5m2_decode.restype = ctypes.c_double
+            L.orc_e5m2_encode_f32.argtypes = [P, I64, P]
+            L.orc_e5m2_encode_f32.restype = None
             L.orc_tgmm.restype = I64
             _lib = L
     return _lib
@@ -83,6 +87,20 @@ def num_threads() -> int:
 
 def e4m3_decode(code: int) -> float:
     return lib().orc_e4m3_decode(code)
+
+
+FMT = {"e4m3": 0, "e5m2": 1}
+
+
+def e5m2_decode(code: int) -> float:
+    return lib().orc_e5m2_decode(code)
+
+
+def e5m2_encode(x: torch.Tensor) -> torch.Tensor:
+    x = x.to(torch.float32).contiguous()
+    out = torch.empty(x.shape, dtype=torch.uint8)
+    lib().orc_e5m2_encode_f32(_p(x), x.numel(), _p(out))
+    return out
 
 
 def e4m3_decode_all() -> torch.Tensor:
@@ -199,7 +217,7 @@ def segment_bound(M: int, E: int) -> int:
     return (M + 127) // 128 + E
 
 
-def tgmm_quantize_tiles(lhs, dout, gs, Smax=None):
+def tgmm_quantize_tiles(lhs, dout, gs, Smax=None, dout_fmt="e4m3"):
     """a7: per-segment per-channel codes and scales (slot layout, see the C
     source). Returns (qx, sx, qd, sd, nseg, bad_reads)."""
     M, K = lhs.shape
@@ -216,11 +234,11 @@ def tgmm_quantize_tiles(lhs, dout, gs, Smax=None):
     nseg = ctypes.c_int64(0)
     bad = lib().orc_tgmm_quantize_tiles(_p(lhs.contiguous()), _p(dout.contiguous()),
                                         M, K, N, E, _p(gs), Smax, _p(qx), _p(sx),
-                                        _p(qd), _p(sd), ctypes.byref(nseg))
+                                        _p(qd), _p(sd), ctypes.byref(nseg), FMT[dout_fmt])
     return qx, sx, qd, sd, nseg.value, bad
 
 
-def tgmm(lhs, dout, gs, experts=None, k_range=None, n_range=None):
+def tgmm(lhs, dout, gs, experts=None, k_range=None, n_range=None, dout_fmt="e4m3"):
     """a8: dW f32 [len(experts) or E, k1 - k0, n1 - n0] for the selected experts
     and block (default: all of it). Returns (dW, bad_reads)."""
     M, K = lhs.shape
@@ -233,5 +251,6 @@ def tgmm(lhs, dout, gs, experts=None, k_range=None, n_range=None):
     nex = E if ex is None else ex.numel()
     dW = torch.full((nex, k1 - k0, n1 - n0), float("nan"), dtype=torch.float32)
     bad = lib().orc_tgmm(_p(lhs.contiguous()), _p(dout.contiguous()), M, K, N, E, _p(gs),
-                         _p(ex), 0 if ex is None else ex.numel(), k0, k1, n0, n1, _p(dW))
+                         _p(ex), 0 if ex is None else ex.numel(), k0, k1, n0, n1, _p(dW),
+                         FMT[dout_fmt])
     return dW, bad

@@ -127,3 +127,70 @@ def test_bf16_single_rounding_from_double(orc):
     assert got == [1.0, 1 + 2.0 ** -7, 1 + 2 * 2.0 ** -7, 1.0]
     big = orc.f64_to_bf16(torch.tensor([3.4e38, float("nan")], dtype=torch.float64))
     assert math.isinf(float(big[0])) and math.isnan(float(big[1]))
+
+
+# --------------------------------------------------------------------- e5m2
+# The tgmm's gradient operand may be e5m2 ("MoE fp8 backward: in-kernel drhs
+# operand quantization + configurable gradient dtype", What). OCP e5m2: bias 15,
+# 2 mantissa bits, subnormals m * 2^-16, exponent 31 = Inf / NaN, max 57344.
+F8E5 = torch.float8_e5m2
+
+
+def e5m2_formula(c: int) -> float:
+    s = -1.0 if c & 0x80 else 1.0
+    e, m = (c >> 2) & 0x1F, c & 0x3
+    if e == 31:
+        return s * math.inf if m == 0 else math.nan
+    if e == 0:
+        return s * m * 2.0 ** -16
+    return s * (1.0 + m / 4.0) * 2.0 ** (e - 15)
+
+
+def test_e5m2_decode_all_codes_match_torch_and_formula(orc):
+    ours = torch.tensor([orc.e5m2_decode(c) for c in range(256)], dtype=torch.float64)
+    theirs = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(F8E5).to(torch.float64)
+    form = torch.tensor([e5m2_formula(c) for c in range(256)], dtype=torch.float64)
+    for ref in (theirs, form):
+        nan = torch.isnan(ref)
+        assert torch.equal(torch.isnan(ours), nan)
+        assert torch.equal(ours[~nan], ref[~nan])
+    assert orc.e5m2_decode(0x7B) == 57344.0 and orc.e5m2_decode(0x01) == 2.0 ** -16
+    assert math.isinf(orc.e5m2_decode(0x7C))
+
+
+def test_e5m2_encode_roundtrip_all_finite_codes(orc):
+    codes = [c for c in range(256) if (c & 0x7F) < 0x7C]
+    vals = torch.tensor([orc.e5m2_decode(c) for c in codes], dtype=torch.float32)
+    got = orc.e5m2_encode(vals)
+    # +0 and -0 both keep their sign
+    assert got.tolist() == codes
+
+
+def test_e5m2_encode_midpoints_round_to_even_code(orc):
+    mids, want = [], []
+    for c in range(0, 0x7B):
+        a, b = orc.e5m2_decode(c), orc.e5m2_decode(c + 1)
+        mids.append((a + b) / 2)            # exact in f32: 3 significant bits
+        want.append(c if c % 2 == 0 else c + 1)
+    got = orc.e5m2_encode(torch.tensor(mids, dtype=torch.float32))
+    assert got.tolist() == want
+    neg = orc.e5m2_encode(-torch.tensor(mids, dtype=torch.float32))
+    assert neg.tolist() == [w | 0x80 for w in want]
+
+
+def test_e5m2_encode_saturates_and_nan(orc):
+    x = torch.tensor([57344.0, 61440.0, 65535.0, 1e30, math.inf, -math.inf, -61440.0],
+                     dtype=torch.float32)
+    assert orc.e5m2_encode(x).tolist() == [0x7B] * 5 + [0xFB, 0xFB]
+    n = orc.e5m2_encode(torch.tensor([math.nan], dtype=torch.float32))
+    assert (int(n[0]) & 0x7F) > 0x7C               # a NaN code
+
+
+@pytest.mark.parametrize("scale", [1e-6, 1e-3, 1.0, 300.0, 40000.0])
+def test_e5m2_encode_matches_torch_on_random_values(orc, scale):
+    g = torch.Generator().manual_seed(int(scale * 7) + 3)
+    x = (torch.randn(200000, generator=g) * scale).to(torch.float32)
+    x = x.clamp(-57344.0, 57344.0)                 # torch overflows to Inf past the max
+    ours = orc.e5m2_encode(x)
+    theirs = x.to(F8E5).view(torch.uint8)
+    assert torch.equal(ours, theirs)

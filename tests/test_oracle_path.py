@@ -352,6 +352,76 @@ def test_tgmm_bruteforce_tiny(orc):
         assert np.array_equal(dW[e].numpy(), ref.astype(np.float32))
 
 
+F8E5 = torch.float8_e5m2
+
+
+def test_tgmm_e5m2_lossless_case_is_textbook_xt_d(orc):
+    """e5m2 gradient operand ("MoE fp8 backward ...", What: configurable gradient
+    dtype): x channels on the e4m3 grid with amax 448 and dout channels on the
+    e5m2 grid with amax 57344 in every segment -> all scales are 1 -> dW_e =
+    X_e^T D_e exactly. dout codes keep |v| >= 2^-6 so every double sum is exact."""
+    M, K, N = 300, 20, 24
+    gs = torch.tensor([100, 150, 0, 40], dtype=torch.int32)
+    g = torch.Generator().manual_seed(4)
+    c = torch.randint(0, 256, (M, K), generator=g, dtype=torch.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x20
+    x = c.view(F8).to(torch.float32)
+    e = torch.randint(0x0C, 0x7C, (M, N), generator=g, dtype=torch.uint8)   # 2^-6 .. 57344
+    e |= (torch.randint(0, 2, (M, N), generator=g, dtype=torch.uint8) << 7)
+    d = e.view(F8E5).to(torch.float32)
+    bounds = [(0, 100), (100, 250), (250, 290)]
+    for a, b in bounds:
+        for t in range(a // 128, (b - 1) // 128 + 1):
+            r = max(a, 128 * t)
+            x[r] = -448.0
+            d[r] = 57344.0
+    x = W.fill_tail_garbage(x.to(torch.bfloat16), 290)
+    d = W.fill_tail_garbage(d.to(torch.bfloat16), 290)
+    dW, bad = orc.tgmm(x, d, gs, dout_fmt="e5m2")
+    assert bad == 0
+    for ex, (a, b) in zip([0, 1, 3], bounds):
+        ref = (x[a:b].double().T @ d[a:b].double()).float()
+        assert torch.equal(dW[ex], ref)
+    assert (dW[2] == 0).all()
+    _, sx, _, sd, nseg, bad = orc.tgmm_quantize_tiles(x, d, gs, dout_fmt="e5m2")
+    assert bad == 0 and (sx[:nseg] == 1.0).all() and (sd[:nseg] == 1.0).all()
+
+
+def test_tgmm_e5m2_bruteforce_tiny(orc):
+    """Plain Python restatement with an e5m2 dout operand: segments, f32
+    per-channel scales max(amax, 1e-12)/57344 (numpy), codes by torch's
+    float8_e5m2 cast, double dot products."""
+    M, K, N = 260, 3, 2
+    gs = [70, 100, 0, 60]
+    x = W.fill_tail_garbage(W.activations(M, K, 23), 230)
+    d = W.cotangent(M, N, 24) * 1000
+    dW, bad = orc.tgmm(x, d, torch.tensor(gs, dtype=torch.int32), dout_fmt="e5m2")
+    assert bad == 0
+    xf, df = x.float().numpy(), d.float().numpy()
+
+    def quant(col, fmax, dt):
+        amax = np.float32(np.abs(col).max())
+        s = np.float32(max(amax, np.float32(1e-12))) / np.float32(fmax)
+        return s, torch.from_numpy((col / s).astype(np.float32)).to(dt).double().numpy()
+
+    off = 0
+    for e, g in enumerate(gs):
+        ref = np.zeros((K, N))
+        a, b = off, off + g
+        off += g
+        if g == 0:
+            assert (dW[e] == 0).all()
+            continue
+        for t in range(a // 128, (b - 1) // 128 + 1):
+            r0, r1 = max(a, 128 * t), min(b, 128 * t + 128)
+            for k in range(K):
+                sk, qk = quant(xf[r0:r1, k], 448.0, F8)
+                for n in range(N):
+                    sn, qn = quant(df[r0:r1, n], 57344.0, F8E5)
+                    ref[k, n] += float(sk) * float(sn) * float(np.dot(qk, qn))
+        assert np.array_equal(dW[e].numpy(), ref.astype(np.float32))
+
+
 def test_tgmm_tail_invariance_locality_empty(orc):
     M, K, N = 512, 32, 16
     gs = torch.tensor([0, 130, 77, 0, 90], dtype=torch.int32)   # T = 297
