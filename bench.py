@@ -452,6 +452,11 @@ def main():
             "tflops": round(flops["wo_dlhs"] / (t_dsw * 1e-3) / 1e12, 1),
             "extra_bytes": "reads gu [M, 2F], writes dgu [M, 2F] instead of dh [M, F]"}
         del dgu_out
+        # wo weight gradient with the e5m2 gradient dtype
+        t_e5 = timeit(lambda: fb.tgmm_drhs_quant(step.h, inp["dy"], inp["gs"], out=step.dw,
+                                                 workspace=step.ws_tg, dout_fmt="e5m2"))
+        extra["wo_dw_e5m2"] = {"ms": round(t_e5, 4), "e4m3_ms": round(per["wo_dw"], 4),
+                               "tflops": round(flops["wo_dw"] / (t_e5 * 1e-3) / 1e12, 1)}
         extra["microbench"] = microbench(fb, timeit, torch.device("cuda", torch.cuda.current_device()))
 
     # ------------------------------------------------------------------ e2e

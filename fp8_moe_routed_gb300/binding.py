@@ -40,7 +40,10 @@ EXPORTS = [
     "fp8moe_tgmm_quantize_tiles", "fp8moe_read_status", "fp8moe_status_string",
     "fp8moe_last_cuda_error", "fp8moe_num_sms", "fp8moe_gmm_silu_fp8_fwd_noalloc",
     "fp8moe_gmm_dlhs_dswiglu_fp8", "fp8moe_gmm_dlhs_dswiglu_fp8_path",
+    "fp8moe_tgmm_drhs_quant_fmt", "fp8moe_tgmm_quantize_tiles_fmt",
 ]
+
+FMT = {"e4m3": 0, "e5m2": 1}
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +89,9 @@ def load(build_if_missing: bool = True):
             "fp8moe_gmm_dlhs_dswiglu_fp8": ([P, I64, I64, P, P, I32, I64, P, P, P, P, SZ, P], I32),
             "fp8moe_gmm_dlhs_dswiglu_fp8_path": ([P, I64, I64, P, P, I32, I64, P, P, P, I32, P],
                                                  I32),
+            "fp8moe_tgmm_drhs_quant_fmt": ([P, P, I64, I64, I64, I32, P, P, P, SZ, I32, P], I32),
+            "fp8moe_tgmm_quantize_tiles_fmt": ([P, P, I64, I64, I64, I32, P, P, P, P, P, I32, P],
+                                               I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -253,8 +259,9 @@ def gmm_dlhs_dswiglu_fp8(dout, codes, scale, gu, group_sizes, out=None,
     return out
 
 
-def tgmm_drhs_quant(lhs, dout, group_sizes, out=None, workspace=None):
-    """Weight gradient f32 [E, K, N] (see fp8moe_tgmm_drhs_quant)."""
+def tgmm_drhs_quant(lhs, dout, group_sizes, out=None, workspace=None, dout_fmt: str = "e4m3"):
+    """Weight gradient f32 [E, K, N] (see fp8moe_tgmm_drhs_quant; dout_fmt
+    "e5m2" quantizes the gradient operand to e5m2, fp8moe_tgmm_drhs_quant_fmt)."""
     L = load()
     _req(lhs, torch.bfloat16, "lhs", 2)
     _req(dout, torch.bfloat16, "dout", 2)
@@ -269,9 +276,14 @@ def tgmm_drhs_quant(lhs, dout, group_sizes, out=None, workspace=None):
     else:
         _req(out, torch.float32, "out", 3)
     ws, wsb = _workspace(OP_TGMM_DRHS_QUANT, M, K, N, E, lhs.device, workspace)
-    _check(L.fp8moe_tgmm_drhs_quant(_ptr(lhs), _ptr(dout), M, K, N, E, _ptr(group_sizes),
-                                    _ptr(out), _ptr(ws), wsb, _stream(lhs.device)),
-           "fp8moe_tgmm_drhs_quant")
+    if dout_fmt == "e4m3":
+        rc = L.fp8moe_tgmm_drhs_quant(_ptr(lhs), _ptr(dout), M, K, N, E, _ptr(group_sizes),
+                                      _ptr(out), _ptr(ws), wsb, _stream(lhs.device))
+    else:
+        rc = L.fp8moe_tgmm_drhs_quant_fmt(_ptr(lhs), _ptr(dout), M, K, N, E, _ptr(group_sizes),
+                                          _ptr(out), _ptr(ws), wsb, FMT[dout_fmt],
+                                          _stream(lhs.device))
+    _check(rc, "fp8moe_tgmm_drhs_quant")
     return out
 
 
@@ -326,7 +338,7 @@ def segment_bound(M: int, E: int) -> int:
     return (M + 127) // 128 + E
 
 
-def tgmm_quantize_tiles(lhs, dout, group_sizes):
+def tgmm_quantize_tiles(lhs, dout, group_sizes, dout_fmt: str = "e4m3"):
     """Parity export of the tgmm operand quantization (slot layout)."""
     L = load()
     _req(lhs, torch.bfloat16, "lhs", 2)
@@ -341,8 +353,9 @@ def tgmm_quantize_tiles(lhs, dout, group_sizes):
     sx = torch.full((S, K), float("nan"), dtype=torch.float32, device=dev)
     qd = torch.zeros(S, 128, N, dtype=torch.uint8, device=dev)
     sd = torch.full((S, N), float("nan"), dtype=torch.float32, device=dev)
-    _check(L.fp8moe_tgmm_quantize_tiles(_ptr(lhs), _ptr(dout), M, K, N, E, _ptr(group_sizes),
-                                        _ptr(qx), _ptr(sx), _ptr(qd), _ptr(sd), _stream(dev)),
+    _check(L.fp8moe_tgmm_quantize_tiles_fmt(_ptr(lhs), _ptr(dout), M, K, N, E, _ptr(group_sizes),
+                                            _ptr(qx), _ptr(sx), _ptr(qd), _ptr(sd), FMT[dout_fmt],
+                                            _stream(dev)),
            "fp8moe_tgmm_quantize_tiles")
     return qx, sx, qd, sd
 

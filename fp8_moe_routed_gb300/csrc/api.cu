@@ -235,10 +235,10 @@ int dlhs_impl(const void* dout, int64_t M, int64_t N, const uint8_t* codes, cons
 
 int tgmm_quantize_impl(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
                        int32_t E, const int32_t* gs, uint8_t* qx, float* sx, uint8_t* qd,
-                       float* sd, cudaStream_t stream, int sms) {
+                       float* sd, cudaStream_t stream, int sms, int d_fmt) {
   cudaError_t e = fp8moe_launch_tgmm_quantize_tiles(lhs, dout, M, (int)K, (int)N, gs, E,
                                                     segment_bound(M, E), qx, sx, qd, sd, sms, 1,
-                                                    stream);
+                                                    d_fmt, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
 }
@@ -315,11 +315,12 @@ int fp8moe_gmm_dlhs_dswiglu_fp8_path(const void* dout, int64_t M, int64_t N, con
   return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
 }
 
-int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
-                           int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
-                           size_t workspace_bytes, fp8moe_stream_t stream) {
+static int tgmm_drhs_impl(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
+                          int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
+                          size_t workspace_bytes, int d_fmt, fp8moe_stream_t stream) {
   int rc = check_common(M, K, N, E);
   if (rc) return rc;
+  if (d_fmt != FP8MOE_FMT_E4M3 && d_fmt != FP8MOE_FMT_E5M2) return FP8MOE_EINVAL;
   if (!dW || !group_sizes) return FP8MOE_EINVAL;
   if (M > 0 && (!lhs || !dout)) return FP8MOE_EINVAL;
   if (!workspace) return FP8MOE_EWORKSPACE;
@@ -334,7 +335,8 @@ int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t
   TgmmWorkspace w = carve_tgmm(workspace, M, K, N, E);
   const int64_t S = segment_bound(M, E);
   if (M > 0) {
-    rc = tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, w.qx, w.sx, w.qd, w.sd, stream, sms);
+    rc = tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, w.qx, w.sx, w.qd, w.sd, stream, sms,
+                            d_fmt);
     if (rc) return rc;
   }
   TgmmArgs a;
@@ -362,9 +364,24 @@ int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t
   a.K = (int)K;
   a.N = (int)N;
   a.E = E;
+  a.d_fmt = d_fmt;
   cudaError_t e = fp8moe_launch_tgmm(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
+}
+
+int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
+                           int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
+                           size_t workspace_bytes, fp8moe_stream_t stream) {
+  return tgmm_drhs_impl(lhs, dout, M, K, N, E, group_sizes, dW, workspace, workspace_bytes,
+                        FP8MOE_FMT_E4M3, stream);
+}
+
+int fp8moe_tgmm_drhs_quant_fmt(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
+                               int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
+                               size_t workspace_bytes, int32_t dout_fmt, fp8moe_stream_t stream) {
+  return tgmm_drhs_impl(lhs, dout, M, K, N, E, group_sizes, dW, workspace, workspace_bytes,
+                        dout_fmt, stream);
 }
 
 int fp8moe_dequantize_fp8_codes(const uint8_t* codes, const float* scale, int32_t E, int64_t K,
@@ -445,8 +462,17 @@ int fp8moe_quantize_rows(const void* lhs, int64_t M, int64_t K, const int32_t* g
 int fp8moe_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int64_t K,
                                int64_t N, int32_t E, const int32_t* group_sizes, uint8_t* qx,
                                float* sx, uint8_t* qd, float* sd, fp8moe_stream_t stream) {
+  return fp8moe_tgmm_quantize_tiles_fmt(lhs, dout, M, K, N, E, group_sizes, qx, sx, qd, sd,
+                                        FP8MOE_FMT_E4M3, stream);
+}
+
+int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M, int64_t K,
+                                   int64_t N, int32_t E, const int32_t* group_sizes, uint8_t* qx,
+                                   float* sx, uint8_t* qd, float* sd, int32_t dout_fmt,
+                                   fp8moe_stream_t stream) {
   int rc = check_common(M, K, N, E);
   if (rc) return rc;
+  if (dout_fmt != FP8MOE_FMT_E4M3 && dout_fmt != FP8MOE_FMT_E5M2) return FP8MOE_EINVAL;
   if (M == 0) return FP8MOE_OK;
   if (!lhs || !dout || !group_sizes || !qx || !sx || !qd || !sd) return FP8MOE_EINVAL;
   if (!aligned16(lhs) || !aligned16(dout) || !aligned16(qx) || !aligned16(qd) ||
@@ -455,7 +481,8 @@ int fp8moe_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int
   int sms = 0;
   rc = device_init(&sms);
   if (rc) return rc;
-  return tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, qx, sx, qd, sd, stream, sms);
+  return tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, qx, sx, qd, sd, stream, sms,
+                            dout_fmt);
 }
 
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags) {

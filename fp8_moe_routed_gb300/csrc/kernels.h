@@ -12,7 +12,8 @@ cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
-                                              int num_sms, int report, cudaStream_t s);
+                                              int num_sms, int report, int d_fmt,
+                                              cudaStream_t s);
 cudaError_t fp8moe_launch_dequantize(const uint8_t* codes, const float* scale, int E, int64_t K,
                                      int64_t N, void* out, int num_sms, cudaStream_t s);
 
@@ -52,6 +53,7 @@ struct TgmmArgs {
   float* dW;              // [E, K, N]
   int64_t M;
   int K, N, E;
+  int d_fmt;              // qd codes: 0 e4m3, 1 e5m2
 };
 cudaError_t fp8moe_launch_tgmm(const TgmmArgs& a, int num_sms, cudaStream_t s);
 

@@ -216,6 +216,14 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Two f32 -> two e5m2 (round to nearest even, saturate to +-57344, NaN -> NaN).
+// lo lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Two e4m3 (low byte first) -> two f16 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;

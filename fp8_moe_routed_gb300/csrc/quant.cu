@@ -8,6 +8,9 @@
 //    cast pass; rows at or past T = sum(group_sizes) are never read.
 //
 //  * tgmm_quantize_tiles_kernel: the weight-gradient operands, per 128-row tile
+//    (the dout operand optionally e5m2, the configurable gradient dtype of
+//    "MoE fp8 backward: in-kernel drhs operand quantization", What: scale =
+//    max(amax, 1e-12) / 57344, codes = e5m2(x / scale))
 //    and per channel, over the rows of one group only ("MoE fp8 backward:
 //    in-kernel drhs operand quantization", What). Codes go to 128-row slots, one
 //    per (tile, group) segment, rows outside the segment zeroed, so the
@@ -30,6 +33,7 @@ namespace fp8moe {
 
 constexpr float kEps = 1e-12f;
 constexpr float kE4m3Max = 448.0f;
+constexpr float kE5m2Max = 57344.0f;
 
 __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t v) {
   uint32_t a = v & 0x7FFF7FFFu, r;
@@ -58,6 +62,18 @@ __device__ __forceinline__ float e4m3_quotient(float x, float s, float r) {
   const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
   const bool near_mid = ((b & 0xFFFFFu) - 0x7FFFCu) < 9u;
   if (near_mid || b < 0x3C800000u) y = __fdiv_rn(x, s);
+  return y;
+}
+
+// The same for e5m2 (2 mantissa bits, bias 15): the boundaries in the normal
+// range are f32 numbers whose low 21 mantissa bits are exactly 0x100000, and
+// the subnormal range is |y| < 2^-14. Past the largest finite value (57344)
+// everything saturates, so the boundary there (61440) needs no care either way.
+__device__ __forceinline__ float e5m2_quotient(float x, float s, float r) {
+  float y = __fmul_rn(x, r);
+  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
+  const bool near_mid = ((b & 0x1FFFFFu) - 0xFFFFCu) < 9u;
+  if (near_mid || b < 0x38800000u) y = __fdiv_rn(x, s);
   return y;
 }
 
@@ -231,7 +247,7 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
     const __nv_bfloat16* __restrict__ lhs, const __nv_bfloat16* __restrict__ dout, int64_t M,
     int K, int N, const int32_t* __restrict__ gs, int E, int64_t Smax,
     uint8_t* __restrict__ qx, float* __restrict__ sx, uint8_t* __restrict__ qd,
-    float* __restrict__ sd, int report) {
+    float* __restrict__ sd, int report, int d_fmt) {
   __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts], s_segbase[kMaxExperts + 1];
   __shared__ int32_t s_T;
   __shared__ __align__(16) uint8_t s_tile[128 * kTQRowBytes];   // [row][128 bf16]
@@ -258,6 +274,8 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
     const int r0 = max(s_begin[e], t * 128), r1 = min(s_end[e], t * 128 + 128);
     const int lo = r0 - t * 128, hi = r1 - t * 128;            // slot rows of the segment
     const bool is_x = ch < ck;
+    const bool e5 = !is_x && d_fmt == 1;                        // e5m2 codes
+    const float fmax = e5 ? kE5m2Max : kE4m3Max;
     const int C = is_x ? K : N;
     const int c0 = (is_x ? ch : ch - ck) * kTQCols;
     const int ncols = min(kTQCols, C - c0);                     // multiple of 16
@@ -294,8 +312,8 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
       uint32_t m2 = s_part[0][tid];
 #pragma unroll
       for (int i = 1; i < 4; ++i) m2 = bf16x2_absmax(m2, s_part[i][tid]);
-      const float s0 = __fdiv_rn(fmaxf(bf16lo_to_f32(m2), kEps), kE4m3Max);
-      const float s1 = __fdiv_rn(fmaxf(bf16hi_to_f32(m2), kEps), kE4m3Max);
+      const float s0 = __fdiv_rn(fmaxf(bf16lo_to_f32(m2), kEps), fmax);
+      const float s1 = __fdiv_rn(fmaxf(bf16hi_to_f32(m2), kEps), fmax);
       s_scale[2 * tid] = s0;
       s_scale[2 * tid + 1] = s1;
       if (2 * tid < ncols) {
@@ -320,10 +338,17 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
           const uint4 x = *reinterpret_cast<const uint4*>(s_tile + rr * kTQRowBytes + piece * 16);
           const uint32_t w[4] = {x.x, x.y, x.z, x.w};
           uint16_t c[4];
+          if (e5) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            c[j] = f32x2_to_e4m3x2(e4m3_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
-                                   e4m3_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+            for (int j = 0; j < 4; ++j)
+              c[j] = f32x2_to_e5m2x2(e5m2_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
+                                     e5m2_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              c[j] = f32x2_to_e4m3x2(e4m3_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
+                                     e4m3_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+          }
           o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
           o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
         }
@@ -363,11 +388,11 @@ cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
-                                              int num_sms, int report, cudaStream_t s) {
+                                              int num_sms, int report, int d_fmt, cudaStream_t s) {
   using namespace fp8moe;
   int grid = num_sms * 6;
   tgmm_quantize_tiles_kernel<<<grid, kTQThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(lhs), static_cast<const __nv_bfloat16*>(dout), M, K, N,
-      gs, E, Smax, qx, sx, qd, sd, report);
+      gs, E, Smax, qx, sx, qd, sd, report, d_fmt);
   return cudaGetLastError();
 }

@@ -30,6 +30,8 @@
 // The 128-wide n tile and four rescale warps per SM sub-partition keep the
 // accumulator in registers (Blackwell budgets registers per group of four warps)
 // and give the rescale enough warps to hide the TMEM and shared-memory latency.
+// The dout operand's codes may be e5m2 (the configurable gradient dtype of the
+// same page); the MMA then reads B as e5m2 (kind::f8f6f4 takes mixed fp8 types).
 // An expert without rows writes zeros.
 #include <cstdint>
 #include <cuda.h>
@@ -79,7 +81,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
 __global__ void __launch_bounds__(kThreads, 1)
 tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmD,
             const float* __restrict__ sx, const float* __restrict__ sd,
-            const int32_t* __restrict__ gs, float* __restrict__ dW, int64_t M, int K, int N, int E) {
+            const int32_t* __restrict__ gs, float* __restrict__ dW, int64_t M, int K, int N, int E,
+            int d_fmt) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -187,7 +190,8 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
     if (lane == 0) {
       // A = qx slot, [K_mma = 128 rows][M_mma = 128 k] -> MN-major, one atom;
       // B = qd slot, [K_mma = 128 rows][N_mma = 128 n] -> MN-major, one atom.
-      constexpr uint32_t idesc = make_idesc(0, 0, 1, 1, kBK, kBN);
+      // B (qd) is e5m2 when the gradient dtype is e5m2; A (qx) is always e4m3
+      const uint32_t idesc = make_idesc(0, d_fmt == 1 ? 1u : 0u, 1, 1, kBK, kBN);
       int st = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -309,6 +313,6 @@ cudaError_t fp8moe_launch_tgmm(const TgmmArgs& a, int num_sms, cudaStream_t s) {
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   tgmm_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(a.tmX, a.tmD, a.sx, a.sd, a.gs, a.dW, a.M,
-                                                    a.K, a.N, a.E);
+                                                    a.K, a.N, a.E, a.d_fmt);
   return cudaGetLastError();
 }

@@ -64,6 +64,13 @@ enum {
   FP8MOE_OP_DEQUANTIZE = 6
 };
 
+/* fp8 formats of the tgmm's dout (gradient) operand -- [DQ] What: the
+ * gradient fp8 dtype is configurable, e5m2 (the recipe's default) or e4m3. */
+enum {
+  FP8MOE_FMT_E4M3 = 0,   /* OCP float8_e4m3fn, max 448 */
+  FP8MOE_FMT_E5M2 = 1    /* OCP float8_e5m2, max 57344 */
+};
+
 /* Bits of the device status word. */
 #define FP8MOE_STATUS_NEGATIVE_GROUP 0x1u    /* some group_sizes[e] < 0 (taken as 0) */
 #define FP8MOE_STATUS_GROUPS_EXCEED_M 0x2u   /* sum(group_sizes) > M (clipped at M) */
@@ -156,6 +163,16 @@ int fp8moe_tgmm_drhs_quant(const void* lhs, const void* dout, int64_t M, int64_t
                            int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
                            size_t workspace_bytes, fp8moe_stream_t stream);
 
+/* fp8moe_tgmm_drhs_quant with the dout operand's fp8 format chosen -- [DQ]
+ * What (configurable gradient dtype).  FP8MOE_FMT_E5M2:
+ *   sd[q,n] = max(max_{m in q} |dout[m,n]|, 1e-12) / 57344, qd = e5m2(dout / sd)
+ * (round to nearest even, saturating at +-57344); lhs stays e4m3 and the MMA
+ * multiplies e4m3 x e5m2.  FP8MOE_FMT_E4M3 is fp8moe_tgmm_drhs_quant.  Any
+ * other dout_fmt: FP8MOE_EINVAL.  Same workspace. */
+int fp8moe_tgmm_drhs_quant_fmt(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
+                               int32_t E, const int32_t* group_sizes, float* dW, void* workspace,
+                               size_t workspace_bytes, int32_t dout_fmt, fp8moe_stream_t stream);
+
 /* dequantize_fp8_codes -- [NQ] Implementation: out[e,k,n] =
  * bf16(f32(codes[e,k,n]) * scale[e,n]) (one f32 multiply, round to nearest
  * even).  out: bf16 [E, K, N]. */
@@ -183,6 +200,13 @@ int fp8moe_quantize_rows(const void* lhs, int64_t M, int64_t K, const int32_t* g
 int fp8moe_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int64_t K,
                                int64_t N, int32_t E, const int32_t* group_sizes, uint8_t* qx,
                                float* sx, uint8_t* qd, float* sd, fp8moe_stream_t stream);
+
+/* fp8moe_tgmm_quantize_tiles with the dout format chosen (FP8MOE_FMT_*): qd
+ * holds e5m2 codes and sd the e5m2 scales when dout_fmt = FP8MOE_FMT_E5M2. */
+int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M, int64_t K,
+                                   int64_t N, int32_t E, const int32_t* group_sizes, uint8_t* qx,
+                                   float* sx, uint8_t* qd, float* sd, int32_t dout_fmt,
+                                   fp8moe_stream_t stream);
 
 /* Waits for `stream`, returns in *flags the OR of the FP8MOE_STATUS_* bits set
  * since the last call, and clears them. */

@@ -227,3 +227,29 @@ def test_balanced_wo_dlhs_dswiglu_sampled(orc):
     ref, _, bad = orc.gmm_dlhs_dswiglu(dy.cpu(), wo_c.cpu(), wo_s.cpu(), gu.cpu(), gs, rows=rows)
     assert bad == 0
     check_bf16(dgu.cpu()[rows], ref[rows], what="balanced wo dlhs+dswiglu")
+
+
+def test_dropless_tgmm_e5m2_blocks_finite_and_tail_blind(orc):
+    """The dropless tgmm with the e5m2 gradient dtype: finite, tail-blind, empty
+    experts zero, oracle blocks of the largest expert and a small one."""
+    E, K, N, M = 32, 7168, 2048, 65536
+    gs = W.group_sizes("dropless", seed=2, E=E)
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, 13, device=DEV), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, 14, device=DEV), T)
+    gsd = gs.to(DEV)
+    dw = fb.tgmm_drhs_quant(x, d, gsd, dout_fmt="e5m2")
+    assert torch.isfinite(dw).all()
+    for e in (gs == 0).nonzero().flatten().tolist():
+        assert (dw[e] == 0).all()
+    x[T:] = float("nan")
+    d[T:] = -3.0e38
+    dw2 = fb.tgmm_drhs_quant(x, d, gsd, dout_fmt="e5m2")
+    assert torch.equal(dw2, dw)
+    del dw2
+    order = torch.argsort(gs, descending=True).tolist()
+    xc, dc = x.cpu(), d.cpu()
+    for e, kr, nr in [(order[0], (128, 256), (1024, 1152)), (order[20], (7040, 7168), (0, 128))]:
+        ref, bad = orc.tgmm(xc, dc, gs, experts=[e], k_range=kr, n_range=nr, dout_fmt="e5m2")
+        assert bad == 0
+        check_f32_rel(dw[e, kr[0]:kr[1], nr[0]:nr[1]], ref[0], what=f"tgmm e5m2 e={e}")

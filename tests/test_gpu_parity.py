@@ -282,6 +282,90 @@ def test_tgmm_quantize_tiles_bit_exact(orc):
     assert torch.equal(sx.cpu()[:nseg], rsx[:nseg]) and torch.equal(sd.cpu()[:nseg], rsd[:nseg])
 
 
+# -------------------------------------------- e5m2 gradient operand (tgmm)
+@pytest.mark.parametrize("M,K,N,E,gs", TGMM_CASES)
+def test_tgmm_e5m2_vs_oracle(orc, M, K, N, E, gs):
+    """The gradient fp8 dtype e5m2 ("MoE fp8 backward ...", What): dout codes
+    e5m2 with max 57344, lhs codes e4m3, e4m3 x e5m2 MMA."""
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=2, M=M, E=E)
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=K + 5), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=N + 6), T)
+    dw = fb.tgmm_drhs_quant(*cuda(x, d, gs), dout_fmt="e5m2")
+    ref, bad = orc.tgmm(x, d, gs, dout_fmt="e5m2")
+    assert bad == 0
+    assert torch.isfinite(dw).all()
+    if T == 0:
+        assert (dw == 0).all()
+    else:
+        check_f32_rel(dw, ref, what="tgmm e5m2")
+        # e5m2 and e4m3 dout give different (coarser) results: the format is live
+        dw4 = fb.tgmm_drhs_quant(*cuda(x, d, gs))
+        assert not torch.equal(dw4, dw)
+
+
+def test_tgmm_quantize_tiles_e5m2_bit_exact(orc):
+    M, K, N = 1024, 512, 256
+    gs = torch.tensor([300, 0, 129, 1, 200, 0], dtype=torch.int32)
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=7), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=8), T)
+    qx, sx, qd, sd = fb.tgmm_quantize_tiles(*cuda(x, d, gs), dout_fmt="e5m2")
+    rqx, rsx, rqd, rsd, nseg, bad = orc.tgmm_quantize_tiles(x, d, gs, dout_fmt="e5m2")
+    assert bad == 0
+    assert torch.equal(qx.cpu()[:nseg], rqx[:nseg]) and torch.equal(qd.cpu()[:nseg], rqd[:nseg])
+    assert torch.equal(sx.cpu()[:nseg], rsx[:nseg]) and torch.equal(sd.cpu()[:nseg], rsd[:nseg])
+
+
+def _e5m2_stress_cols(n_cols=64, seed=19):
+    """Column c holds every bf16 magnitude of the 31 binades below a random amax,
+    both signs, shuffled down 8192 rows: per 128-row segment x / scale sweeps the
+    e5m2 rounding boundaries down into its subnormal range."""
+    g = torch.Generator().manual_seed(seed)
+    cols = []
+    for c in range(n_cols):
+        e = int(torch.randint(-20, 20, (1,), generator=g))
+        mant = int(torch.randint(0, 128, (1,), generator=g))
+        hi_bits = ((e + 127) << 7) | mant
+        lo_bits = (e - 31 + 127) << 7
+        mags = torch.arange(lo_bits, hi_bits + 1, dtype=torch.int32)
+        vals = torch.cat([mags, mags | 0x8000]).to(torch.int16)
+        col = torch.zeros(8192, dtype=torch.int16)
+        col[:vals.numel()] = vals[torch.randperm(vals.numel(), generator=g)]
+        cols.append(col)
+    return torch.stack(cols, dim=1).contiguous().view(torch.bfloat16)
+
+
+def test_tgmm_quantize_e5m2_quotient_stress_bit_exact(orc):
+    d = _e5m2_stress_cols()
+    M = d.shape[0]
+    lhs = W.activations(M, 32, 4)
+    gs = torch.tensor([4000, 4192], dtype=torch.int32)
+    qx, sx, qd, sd = fb.tgmm_quantize_tiles(*cuda(lhs, d, gs), dout_fmt="e5m2")
+    rqx, rsx, rqd, rsd, nseg, bad = orc.tgmm_quantize_tiles(lhs, d, gs, dout_fmt="e5m2")
+    assert bad == 0
+    assert torch.equal(sd.cpu()[:nseg], rsd[:nseg]) and torch.equal(qd.cpu()[:nseg], rqd[:nseg])
+    assert torch.equal(sx.cpu()[:nseg], rsx[:nseg]) and torch.equal(qx.cpu()[:nseg], rqx[:nseg])
+    # the sweep reaches the e5m2 subnormal codes (exponent field 0, nonzero)
+    sub = ((rqd[:nseg] & 0x7C) == 0) & ((rqd[:nseg] & 0x03) != 0)
+    assert int(sub.sum()) > 100
+
+
+def test_tgmm_rejects_unknown_dout_format():
+    x = torch.zeros(128, 64, dtype=torch.bfloat16, device=DEV)
+    d = torch.zeros(128, 64, dtype=torch.bfloat16, device=DEV)
+    gs = torch.tensor([128], dtype=torch.int32, device=DEV)
+    out = torch.empty(1, 64, 64, dtype=torch.float32, device=DEV)
+    L = fb.load()
+    ws = torch.empty(fb.workspace_size(fb.OP_TGMM_DRHS_QUANT, 128, 64, 64, 1), dtype=torch.uint8,
+                     device=DEV)
+    rc = L.fp8moe_tgmm_drhs_quant_fmt(fb._ptr(x), fb._ptr(d), 128, 64, 64, 1, fb._ptr(gs),
+                                      fb._ptr(out), fb._ptr(ws), ws.numel(), 2, fb._stream(x.device))
+    assert rc == -1
+
+
 # --------------------------------------------------------- BF16 comparison
 @pytest.mark.parametrize("swiglu", [True, False])
 def test_bf16_gmm_vs_float64(orc, swiglu):
