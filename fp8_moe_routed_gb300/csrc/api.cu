@@ -24,6 +24,7 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int cuda_fail(cudaError_t e) {
@@ -64,6 +65,7 @@ int device_init(int* sms) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -155,8 +157,6 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   if (rc) return rc;
   uint8_t* q = static_cast<uint8_t*>(ws);
   float* sx = reinterpret_cast<float*>(q + round_up((size_t)M * (size_t)K, 256));
-  cudaError_t e = fp8moe_launch_quantize_rows(lhs, M, (int)K, gs, E, q, sx, sms, 1, stream);
-  if (e != cudaSuccess) return cuda_fail(e);
   GmmFwdArgs a;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
@@ -183,6 +183,11 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   a.N = (int)N;
   a.E = E;
   a.swiglu = swiglu;
+  cudaError_t e = fp8moe_launch_quantize_rows(lhs, M, (int)K, gs, E, 0, E, q, sx, sms, 8, 1,
+                                              stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  a.e0 = 0;
+  a.e1 = E;
   e = fp8moe_launch_gmm_fp8_fwd(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
@@ -437,6 +442,8 @@ int fp8moe_gmm_bf16_fwd(const void* lhs, int64_t M, int64_t K, const void* w, in
   a.N = (int)N;
   a.E = E;
   a.swiglu = swiglu ? 1 : 0;
+  a.e0 = 0;
+  a.e1 = E;
   cudaError_t e = fp8moe_launch_gmm_bf16_fwd(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
@@ -454,7 +461,8 @@ int fp8moe_quantize_rows(const void* lhs, int64_t M, int64_t K, const int32_t* g
   int sms = 0;
   rc = device_init(&sms);
   if (rc) return rc;
-  cudaError_t e = fp8moe_launch_quantize_rows(lhs, M, (int)K, group_sizes, E, q, sx, sms, 1, stream);
+  cudaError_t e = fp8moe_launch_quantize_rows(lhs, M, (int)K, group_sizes, E, 0, E, q, sx, sms, 8,
+                                              1, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
 }

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const float* __restrict__ sx, const float* __restrict__ scale,
                const int32_t* __restrict__ gs, __nv_bfloat16* __restrict__ out, int64_t M, int K,
-               int N, int E) {
+               int N, int E, int e0, int e1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -120,7 +120,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int base = 0; base < E; base += 32) {
       int e = base + lane;
       int32_t n = 0;
-      if (e < E) n = (((s.end[e] - s.begin[e] + kBM - 1) / kBM + 1) / 2) * nt;
+      if (e >= e0 && e < e1) n = (((s.end[e] - s.begin[e] + kBM - 1) / kBM + 1) / 2) * nt;
       int32_t incl = n;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -382,7 +382,7 @@ cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   err = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sx, a.scale, a.gs,
-                           static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N, a.E);
+                           static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N, a.E, a.e0, a.e1);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

@@ -54,6 +54,46 @@ __device__ __forceinline__ void load_groups_warp0(const int32_t* __restrict__ gs
   }
 }
 
+// Warp 0 of the block writes the row range [*s_lo, *s_hi) of experts [e0, e1)
+// (clipped at M like load_groups_warp0) without per-expert arrays; the caller
+// synchronizes afterwards. report != 0: also record clamping in the status word.
+__device__ __forceinline__ void group_row_range_warp0(const int32_t* __restrict__ gs, int E,
+                                                      int64_t M, int e0, int e1, int32_t* s_lo,
+                                                      int32_t* s_hi, int report) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int64_t before = 0, upto = 0, total = 0;   // sums over e < e0, e < e1, all e
+  bool neg = false;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    int64_t g = 0;
+    if (e < E) {
+      const int32_t v = __ldg(gs + e);
+      if (v < 0) neg = true;
+      g = v < 0 ? 0 : v;
+    }
+    int64_t a = e < e0 ? g : 0, b = e < e1 ? g : 0, c = g;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, d);
+      b += __shfl_xor_sync(0xffffffffu, b, d);
+      c += __shfl_xor_sync(0xffffffffu, c, d);
+    }
+    before += a;
+    upto += b;
+    total += c;
+  }
+  neg = __any_sync(0xffffffffu, neg);
+  if (lane == 0) {
+    *s_lo = (int32_t)(before < M ? before : M);
+    *s_hi = (int32_t)(upto < M ? upto : M);
+    if (report) {
+      if (neg) status_set(kStatusNegativeGroup);
+      if (total > M) status_set(kStatusGroupsExceedM);
+    }
+  }
+}
+
 // Given prefix[0..E] (ascending), the e with prefix[e] <= u < prefix[e+1].
 __device__ __forceinline__ int find_bucket(const int32_t* prefix, int E, int32_t u) {
   int lo = 0, hi = E;   // invariant: prefix[lo] <= u < prefix[hi]

@@ -6,9 +6,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+// Rows of experts [e0, e1); ctas_per_sm bounds the grid (resident CTAs per SM).
 cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const int32_t* gs,
-                                        int E, uint8_t* q, float* sx, int num_sms, int report,
-                                        cudaStream_t s);
+                                        int E, int e0, int e1, uint8_t* q, float* sx, int num_sms,
+                                        int ctas_per_sm, int report, cudaStream_t s);
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
@@ -27,6 +28,7 @@ struct GmmFwdArgs {
   void* out;              // bf16 [M, Nout]
   int64_t M;
   int K, N, E, swiglu;
+  int e0, e1;             // only the units of experts [e0, e1)
 };
 cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);
 cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);

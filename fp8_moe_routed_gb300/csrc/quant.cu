@@ -16,9 +16,9 @@
 //    per (tile, group) segment, rows outside the segment zeroed, so the
 //    contraction kernel can TMA whole slots without masking.
 //
-// Both produce exactly the codes of RN_e4m3(RN_f32(x / scale)) (see
-// e4m3_quotient: a reciprocal multiply, with the IEEE division taken wherever
-// the two could round differently) and cast with cvt.rn.satfinite, so codes and
+// Both produce exactly the codes of RN_fp8(RN_f32(x / scale)) (see quotient_x2:
+// two reciprocal multiplies that bracket the quotient, with the IEEE division
+// taken when their codes differ) cast with cvt.rn.satfinite, so codes and
 // scales are bit-exact with a plain f32 reading of the definition. The scale
 // itself is always an IEEE division.
 #include <cstdint>
@@ -45,49 +45,47 @@ __device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t v) {
   return fmaxf(bf16lo_to_f32(v), bf16hi_to_f32(v));
 }
 
-// A value whose e4m3 rounding equals that of the correctly rounded f32 quotient
-// RN(x / s). r = RN(1 / s).
-//   y = RN(x * r) = (x / s)(1 + d), |d| <= 2^-23 + 2^-48, so y is within 3 f32
-//   ulps of RN(x / s). Rounding to e4m3 can only differ between the two when a
-//   rounding boundary lies between them. In the normal e4m3 range the
-//   boundaries are the midpoints between 4-significant-bit values: f32 numbers
-//   whose low 20 mantissa bits are exactly 0x80000. Grid points themselves and
-//   powers of two are not boundaries, and everything past 448 saturates. So y is
-//   returned unless its low 20 bits are within 4 of 0x80000 or |y| < 2^-6 (the
-//   e4m3 subnormal range, where the boundaries sit elsewhere); then the exact
-//   IEEE quotient is computed. Infinite and NaN inputs take the fast path and
-//   convert exactly as the quotient would (saturate, NaN).
-__device__ __forceinline__ float e4m3_quotient(float x, float s, float r) {
-  float y = __fmul_rn(x, r);
-  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
-  const bool near_mid = ((b & 0xFFFFFu) - 0x7FFFCu) < 9u;
-  if (near_mid || b < 0x3C800000u) y = __fdiv_rn(x, s);
-  return y;
+// Codes of the correctly rounded f32 quotients RN(x0 / s), RN(x1 / s), two per
+// conversion, from rl = RN(r * (1 - 2^-20)) and rh = RN(r * (1 + 2^-20)),
+// r = RN(1 / s).
+//   r is within 2^-24 of 1 / s (relative), rl and rh add 2^-24 each, and the
+//   products another 2^-24: x * rl and x * rh (as computed) lie more than 2^-21
+//   below and above x / s, and RN(x / s) within 2^-24 of it, so RN(x / s) is
+//   always between the two ends. Rounding to the fp8 grid (nearest, saturating)
+//   is monotonic: when both ends give the same code, every value between them
+//   does, RN(x / s) included. Otherwise a rounding boundary lies within ~2^-20
+//   of x / s (rare) and the exact IEEE quotients are converted instead. Below
+//   the f32 normal range the relative bounds fail, but such quotients and both
+//   ends then round to the zero code anyway. NaN and infinite x give the codes
+//   the quotient would (NaN; saturation).
+template <bool E5M2>
+__device__ __forceinline__ uint16_t cvt_x2(float a, float b) {
+  return E5M2 ? f32x2_to_e5m2x2(a, b) : f32x2_to_e4m3x2(a, b);
 }
 
-// The same for e5m2 (2 mantissa bits, bias 15): the boundaries in the normal
-// range are f32 numbers whose low 21 mantissa bits are exactly 0x100000, and
-// the subnormal range is |y| < 2^-14. Past the largest finite value (57344)
-// everything saturates, so the boundary there (61440) needs no care either way.
-__device__ __forceinline__ float e5m2_quotient(float x, float s, float r) {
-  float y = __fmul_rn(x, r);
-  const uint32_t b = __float_as_uint(y) & 0x7FFFFFFFu;
-  const bool near_mid = ((b & 0x1FFFFFu) - 0xFFFFCu) < 9u;
-  if (near_mid || b < 0x38800000u) y = __fdiv_rn(x, s);
-  return y;
+template <bool E5M2>
+__device__ __forceinline__ uint16_t quotient_x2(float x0, float x1, float s0, float s1, float rl0,
+                                                float rl1, float rh0, float rh1) {
+  const uint16_t lo = cvt_x2<E5M2>(__fmul_rn(x0, rl0), __fmul_rn(x1, rl1));
+  const uint16_t hi = cvt_x2<E5M2>(__fmul_rn(x0, rh0), __fmul_rn(x1, rh1));
+  if (lo == hi) return lo;
+  return cvt_x2<E5M2>(__fdiv_rn(x0, s0), __fdiv_rn(x1, s1));
+}
+
+__device__ __forceinline__ void bracket(float s, float& rl, float& rh) {
+  const float r = __frcp_rn(s);
+  rl = __fmul_rn(r, 1.0f - 0x1p-20f);
+  rh = __fmul_rn(r, 1.0f + 0x1p-20f);
 }
 
 // 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2).
-__device__ __forceinline__ uint2 quant8(uint4 v, float s, float r) {
+__device__ __forceinline__ uint2 quant8(uint4 v, float s, float rl, float rh) {
   uint2 o;
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint16_t c[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo = e4m3_quotient(bf16lo_to_f32(w[i]), s, r);
-    float hi = e4m3_quotient(bf16hi_to_f32(w[i]), s, r);
-    c[i] = f32x2_to_e4m3x2(lo, hi);
-  }
+  for (int i = 0; i < 4; ++i)
+    c[i] = quotient_x2<false>(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), s, s, rl, rl, rh, rh);
   o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
   o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
   return o;
@@ -103,13 +101,12 @@ constexpr int kQThreads = 256;
 template <int CPT>
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
-    int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
-  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
-  __shared__ int32_t s_T;
+    int E, int e0, int e1, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
+  __shared__ int32_t s_lo, s_hi;
   __shared__ float s_red[2][kQThreads / 32];
-  load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
+  group_row_range_warp0(gs, E, M, e0, e1, &s_lo, &s_hi, report && blockIdx.x == 0);
   __syncthreads();
-  const int T = s_T;
+  const int64_t lo = s_lo, T = s_hi;   // rows [lo, T) of experts [e0, e1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = K >> 3;   // K % 8 == 0
   int buf = 0;
@@ -118,15 +115,15 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
   uint4 nxt[CPT];
 #pragma unroll
   for (int i = 0; i < CPT; ++i) nxt[i] = make_uint4(0u, 0u, 0u, 0u);
-  if ((int64_t)blockIdx.x < T) {
-    const uint4* row = reinterpret_cast<const uint4*>(lhs + (int64_t)blockIdx.x * K);
+  if (lo + blockIdx.x < T) {
+    const uint4* row = reinterpret_cast<const uint4*>(lhs + (lo + blockIdx.x) * K);
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = threadIdx.x + kQThreads * i;
       if (c < nchunk) nxt[i] = __ldg(row + c);
     }
   }
-  for (int64_t m = blockIdx.x; m < T; m += gridDim.x) {
+  for (int64_t m = lo + blockIdx.x; m < T; m += gridDim.x) {
     uint4 v[CPT];
 #pragma unroll
     for (int i = 0; i < CPT; ++i) v[i] = nxt[i];
@@ -159,12 +156,13 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[buf][w]);
     buf ^= 1;   // the next row reduces into the other buffer: no second barrier needed
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
-    const float rs = __frcp_rn(s);
+    float rl, rh;
+    bracket(s, rl, rh);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
       const int c = threadIdx.x + kQThreads * i;
-      if (c < nchunk) qrow[c] = quant8(v[i], s, rs);
+      if (c < nchunk) qrow[c] = quant8(v[i], s, rl, rh);
     }
     if (threadIdx.x == 0) sx[m] = s;
   }
@@ -174,17 +172,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
 // row (L2 hit).
 __global__ void __launch_bounds__(kQThreads) quantize_rows_stream_kernel(
     const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
-    int E, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
-  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts];
-  __shared__ int32_t s_T;
+    int E, int e0, int e1, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
+  __shared__ int32_t s_lo, s_hi;
   __shared__ float s_red[2][kQThreads / 32];
-  load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
+  group_row_range_warp0(gs, E, M, e0, e1, &s_lo, &s_hi, report && blockIdx.x == 0);
   __syncthreads();
-  const int T = s_T;
+  const int64_t lo = s_lo, T = s_hi;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = K >> 3;
   int buf = 0;
-  for (int64_t m = blockIdx.x; m < T; m += gridDim.x) {
+  for (int64_t m = lo + blockIdx.x; m < T; m += gridDim.x) {
     const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
     uint32_t amax2 = 0;
     for (int c = threadIdx.x; c < nchunk; c += kQThreads) {
@@ -205,8 +202,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_stream_kernel(
     buf ^= 1;
     const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
     uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
-    const float rs = __frcp_rn(s);
-    for (int c = threadIdx.x; c < nchunk; c += kQThreads) qrow[c] = quant8(__ldg(row + c), s, rs);
+    float rl, rh;
+    bracket(s, rl, rh);
+    for (int c = threadIdx.x; c < nchunk; c += kQThreads) qrow[c] = quant8(__ldg(row + c), s, rl, rh);
     if (threadIdx.x == 0) sx[m] = s;
   }
 }
@@ -324,11 +322,11 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
     __syncthreads();
     // cast: every slot row is written, rows outside the segment as zeros
     if (pin) {
-      float sc[8], rc[8];
+      float sc[8], rl[8], rh[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         sc[j] = s_scale[piece * 8 + j];
-        rc[j] = __frcp_rn(sc[j]);
+        bracket(sc[j], rl[j], rh[j]);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -341,13 +339,15 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
           if (e5) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              c[j] = f32x2_to_e5m2x2(e5m2_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
-                                     e5m2_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+              c[j] = quotient_x2<true>(bf16lo_to_f32(w[j]), bf16hi_to_f32(w[j]), sc[2 * j],
+                                       sc[2 * j + 1], rl[2 * j], rl[2 * j + 1], rh[2 * j],
+                                       rh[2 * j + 1]);
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              c[j] = f32x2_to_e4m3x2(e4m3_quotient(bf16lo_to_f32(w[j]), sc[2 * j], rc[2 * j]),
-                                     e4m3_quotient(bf16hi_to_f32(w[j]), sc[2 * j + 1], rc[2 * j + 1]));
+              c[j] = quotient_x2<false>(bf16lo_to_f32(w[j]), bf16hi_to_f32(w[j]), sc[2 * j],
+                                        sc[2 * j + 1], rl[2 * j], rl[2 * j + 1], rh[2 * j],
+                                        rh[2 * j + 1]);
           }
           o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
           o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
@@ -365,23 +365,23 @@ FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_quant)
 
 // ------------------------------------------------------------------ launchers
 cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const int32_t* gs,
-                                        int E, uint8_t* q, float* sx, int num_sms, int report,
-                                        cudaStream_t s) {
+                                        int E, int e0, int e1, uint8_t* q, float* sx, int num_sms,
+                                        int ctas_per_sm, int report, cudaStream_t s) {
   using namespace fp8moe;
-  // Up to 8 row-CTAs resident per SM; the grid strides over the rows.
-  int64_t cap = (int64_t)num_sms * 8;
+  // Up to ctas_per_sm row-CTAs resident per SM; the grid strides over the rows.
+  int64_t cap = (int64_t)num_sms * ctas_per_sm;
   int grid = (int)(M < cap ? M : cap);
   if (grid < 1) grid = 1;
   const auto* x = static_cast<const __nv_bfloat16*>(lhs);
   const int cpt = (K / 8 + kQThreads - 1) / kQThreads;
   if (cpt <= 1)
-    quantize_rows_kernel<1><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+    quantize_rows_kernel<1><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
   else if (cpt <= 2)
-    quantize_rows_kernel<2><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+    quantize_rows_kernel<2><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
   else if (cpt <= 4)
-    quantize_rows_kernel<4><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+    quantize_rows_kernel<4><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
   else
-    quantize_rows_stream_kernel<<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, q, sx, report);
+    quantize_rows_stream_kernel<<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
   return cudaGetLastError();
 }
 
