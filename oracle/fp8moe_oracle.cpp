@@ -241,6 +241,21 @@ void quantize_one_row(const uint16_t* x, int64_t K, uint8_t* q, float* s_out) {
   *s_out = s;
 }
 
+// One row with one bf16-valued scale per block of `block` columns (reading in
+// the comment above orc_gmm_fwd_block).
+void quantize_one_row_block(const uint16_t* x, int64_t K, int64_t block, uint8_t* q,
+                            float* sb) {
+  const int64_t nb = (K + block - 1) / block;
+  for (int64_t b = 0; b < nb; ++b) {
+    const int64_t k0 = b * block, k1 = std::min(K, k0 + block);
+    float amax = 0.0f;
+    for (int64_t k = k0; k < k1; ++k) amax = std::max(amax, std::fabs(bf16_to_f32(x[k])));
+    const float s = bf16_to_f32(f32_to_bf16_rne(std::max(amax, kEps) / kE4m3Max));
+    for (int64_t k = k0; k < k1; ++k) q[k] = e4m3_encode(bf16_to_f32(x[k]) / s);
+    sb[b] = s;
+  }
+}
+
 double silu(double z) { return z / (1.0 + std::exp(-z)); }
 
 }  // namespace
@@ -414,6 +429,96 @@ int64_t orc_gmm_dlhs(const uint16_t* dout, int64_t M, int64_t N,
         dlhs[m * K + k] = f64_to_bf16_rne(acc);
         if (dlhs_f64) dlhs_f64[m * K + k] = acc;
       }
+    }
+  }
+  return bad.load();
+}
+
+// ----- per-512-column block quantization (see quantize_one_row_block) -------
+int64_t orc_quantize_rows_block(const uint16_t* lhs, int64_t M, int64_t K, int64_t block,
+                                const int32_t* gs, int32_t E, uint8_t* q, float* sb) {
+  Groups g(gs, E, M);
+  std::atomic<int64_t> bad{0};
+  RowGuard guard{g.T, &bad};
+  const int64_t nb = (K + block - 1) / block;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t m = 0; m < g.T; ++m) {
+    if (!guard.ok(m)) continue;
+    quantize_one_row_block(lhs + m * K, K, block, q + m * K, sb + m * nb);
+  }
+  return bad.load();
+}
+
+// ----- per-512-column block activation quantization, bf16 accumulation -------
+// [NQ] Implementation and its review thread: an ops-level option quantizes the
+// activation with one bf16 scale per 512-column block (lhs_quant_block_size
+// 512, the earlier default) and accumulates across K blocks in bf16; the
+// production path is the full-K f32 scale with f32 accumulation. The pages do
+// not spell out the rounding points; the reading taken here:
+//   per row m and block b = columns [512 b, min(512 b + 512, K)):
+//     s[m, b] = bf16( max(amax over the block, 1e-12) / 448 )   (f32 division,
+//               then round to nearest even to bf16; kept as its f32 value)
+//     q[m, k] = e4m3(x[m, k] / s[m, b])                          (f32 division)
+//   forward: acc = 0 (bf16); for each block b in order:
+//     d_b = RN_f32( sum_{k in b} q[m, k] * w[e, k, n] )  (the f32 block product)
+//     acc = bf16( acc + d_b * s[m, b] )                   (one rounding to bf16)
+//   y = acc * sw[e, n] (then SwiGLU as the full-K path), rounded once to bf16.
+// acc_max (optional, [M, N]) receives max |acc| over the blocks: the scale of
+// the rounding steps, from which a tolerance follows.
+int64_t orc_gmm_fwd_block(const uint16_t* lhs, int64_t M, int64_t K, int64_t block,
+                          const uint8_t* codes, const float* scale, int32_t E, int64_t N,
+                          const int32_t* gs, int32_t silu_flag, const int64_t* rows,
+                          int64_t nrows, uint16_t* out, double* out_f64, double* acc_max) {
+  Groups g(gs, E, M);
+  std::atomic<int64_t> bad{0};
+  RowGuard guard{g.T, &bad};
+  const int64_t Nout = silu_flag ? N / 2 : N;
+  const int64_t nb = (K + block - 1) / block;
+  auto expert_of = [&](int64_t m) -> int32_t {
+    for (int32_t e = 0; e < E; ++e) if (m >= g.begin[e] && m < g.end[e]) return e;
+    return -1;
+  };
+  std::vector<int64_t> all;
+  if (!rows) { all.resize(g.T); for (int64_t m = 0; m < g.T; ++m) all[m] = m; rows = all.data(); nrows = g.T; }
+#pragma omp parallel
+  {
+    std::vector<uint8_t> qrow(K);
+    std::vector<float> sb(nb);
+    std::vector<double> dot(N), y(N), amx(N);
+    std::vector<uint16_t> acc(N);
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t i = 0; i < nrows; ++i) {
+      const int64_t m = rows[i];
+      if (!guard.ok(m)) continue;
+      const int32_t e = expert_of(m);
+      if (e < 0) continue;
+      quantize_one_row_block(lhs + m * K, K, block, qrow.data(), sb.data());
+      const uint8_t* w = codes + (int64_t)e * K * N;
+      for (int64_t n = 0; n < N; ++n) { acc[n] = 0; amx[n] = 0.0; }
+      for (int64_t b = 0; b < nb; ++b) {
+        for (int64_t n = 0; n < N; ++n) dot[n] = 0.0;
+        for (int64_t k = b * block; k < std::min(K, b * block + block); ++k) {
+          const double a = e4m3_decode(qrow[k]);
+          if (a == 0.0) continue;
+          const uint8_t* wr = w + k * N;
+          for (int64_t n = 0; n < N; ++n) dot[n] += a * e4m3_decode(wr[n]);   // exact
+        }
+        for (int64_t n = 0; n < N; ++n) {
+          const double d = (double)(float)dot[n];                   // f32 block product
+          const double v = (double)bf16_to_f32(acc[n]) + d * (double)sb[b];
+          acc[n] = f64_to_bf16_rne(v);
+          amx[n] = std::max(amx[n], std::fabs((double)bf16_to_f32(acc[n])));
+        }
+      }
+      for (int64_t n = 0; n < N; ++n)
+        y[n] = (double)bf16_to_f32(acc[n]) * (double)scale[(int64_t)e * N + n];
+      for (int64_t j = 0; j < Nout; ++j) {
+        const double v = silu_flag ? silu(y[j]) * y[Nout + j] : y[j];
+        out[m * Nout + j] = f64_to_bf16_rne(v);
+        if (out_f64) out_f64[m * Nout + j] = v;
+      }
+      if (acc_max)
+        for (int64_t n = 0; n < N; ++n) acc_max[m * N + n] = amx[n];
     }
   }
   return bad.load();

@@ -58,6 +58,11 @@ def lib():
             L.orc_dequantize.argtypes = [P, P, I32, I64, I64, P]
             L.orc_gmm_dlhs.argtypes = [P, I64, I64, P, P, I32, I64, P, P, I64, P, P]
             L.orc_dswiglu.argtypes = [P, P, I64, I64, P, I64, P, P]
+            L.orc_quantize_rows_block.argtypes = [P, I64, I64, I64, P, I32, P, P]
+            L.orc_quantize_rows_block.restype = I64
+            L.orc_gmm_fwd_block.argtypes = [P, I64, I64, I64, P, P, I32, I64, P, I32, P, I64,
+                                            P, P, P]
+            L.orc_gmm_fwd_block.restype = I64
             L.orc_dswiglu.restype = None
             L.orc_gmm_dlhs.restype = I64
             L.orc_tgmm_quantize_tiles.argtypes = [P, P, I64, I64, I64, I32, P, I64,
@@ -182,6 +187,38 @@ def gmm_dlhs(dout, codes, scale, gs, rows=None, fill=None, want_f64=False):
                              _p(scale.contiguous()), E, K, _p(gs), _p(r),
                              0 if r is None else r.numel(), _p(out), _p(out64))
     return out.view(torch.bfloat16), out64, bad
+
+
+def quantize_rows_block(lhs, gs, block=512, fill_q=0, fill_s=float("nan")):
+    """Per-512-column block quantization: codes u8 [M, K], bf16-valued f32
+    scales [M, ceil(K / block)] for rows < T (others keep the fill)."""
+    M, K = lhs.shape
+    nb = (K + block - 1) // block
+    q = torch.full((M, K), fill_q, dtype=torch.uint8)
+    sb = torch.full((M, nb), fill_s, dtype=torch.float32)
+    gs = _gs(gs)
+    bad = lib().orc_quantize_rows_block(_p(lhs.contiguous()), M, K, block, _p(gs), gs.numel(),
+                                        _p(q), _p(sb))
+    return q, sb, bad
+
+
+def gmm_fwd_block(lhs, codes, scale, gs, silu: bool, block=512, rows=None, fill=None,
+                  want_f64=False, want_acc_max=False):
+    """Forward GMM with per-block bf16 activation scales and bf16 accumulation
+    across blocks. Returns (out, out_f64, acc_max, bad)."""
+    M, K = lhs.shape
+    E, K2, N = codes.shape
+    assert K2 == K
+    Nout = N // 2 if silu else N
+    out = torch.full((M, Nout), 0 if fill is None else fill, dtype=torch.int16)
+    out64 = torch.full((M, Nout), float("nan"), dtype=torch.float64) if want_f64 else None
+    amx = torch.full((M, N), float("nan"), dtype=torch.float64) if want_acc_max else None
+    gs = _gs(gs)
+    r = None if rows is None else rows.to(torch.int64).contiguous()
+    bad = lib().orc_gmm_fwd_block(_p(lhs.contiguous()), M, K, block, _p(codes.contiguous()),
+                                  _p(scale.contiguous()), E, N, _p(gs), 1 if silu else 0, _p(r),
+                                  0 if r is None else r.numel(), _p(out), _p(out64), _p(amx))
+    return out.view(torch.bfloat16), out64, amx, bad
 
 
 def dswiglu(dh_f64, gu, rows=None, fill=None, want_f64=False):

@@ -229,6 +229,93 @@ def test_dlhs_matches_float64_matmul_per_group(orc):
     assert (out.view(torch.int16)[80:] == 0x7BCD).all()
 
 
+# ----------------------------------- per-512 block quantization (NEXT-3)
+def test_block_quant_scales_and_codes_match_torch(orc):
+    """s[m, b] = bf16(max(amax over the block, 1e-12) / 448) in f32 then bf16 (torch),
+    codes = torch's float8_e4m3fn cast of x / s; K = 1280 has a partial last block."""
+    M, K = 24, 1280
+    x = W.activations(M, K, 41)
+    x[3, 512:1024] = 0.0                                     # an all-zero block
+    gs = torch.tensor([10, 14], dtype=torch.int32)
+    q, sb, bad = orc.quantize_rows_block(x, gs)
+    assert bad == 0 and sb.shape == (M, 3)
+    xf = x.float()
+    for b, (k0, k1) in enumerate([(0, 512), (512, 1024), (1024, 1280)]):
+        amax = xf[:, k0:k1].abs().amax(dim=1)
+        s = (torch.clamp(amax, min=1e-12) / 448.0).to(torch.bfloat16).float()
+        assert torch.equal(sb[:, b], s)
+        ref = (xf[:, k0:k1] / s[:, None]).to(F8).view(torch.uint8)
+        assert torch.equal(q[:, k0:k1], ref)
+    assert sb[3, 1].item() == torch.tensor(1e-12 / 448.0).to(torch.bfloat16).float().item()
+
+
+def test_block_quant_blocks_are_independent(orc):
+    M, K = 8, 1536
+    x = W.activations(M, K, 42)
+    gs = torch.tensor([M], dtype=torch.int32)
+    q, sb, _ = orc.quantize_rows_block(x, gs)
+    x2 = x.clone()
+    x2[:, 600:700] *= 37.0                                   # only block 1 changes
+    q2, sb2, _ = orc.quantize_rows_block(x2, gs)
+    assert torch.equal(q[:, :512], q2[:, :512]) and torch.equal(q[:, 1024:], q2[:, 1024:])
+    assert torch.equal(sb[:, [0, 2]], sb2[:, [0, 2]]) and not torch.equal(sb[:, 1], sb2[:, 1])
+
+
+def test_gmm_fwd_block_restated_in_python(orc):
+    """Plain-Python restatement on a tiny case (K = 1280: blocks 512, 512, 256):
+    the exact block product rounded to f32, acc = bf16(acc + d * s) with one
+    rounding (the oracle's pinned f64 -> bf16), then * sw and one last rounding."""
+    M, K, N, E = 6, 1280, 8, 2
+    gs = torch.tensor([2, 4], dtype=torch.int32)
+    x = W.activations(M, K, 43)
+    codes, scale = W.fp8_weights(E, K, N, 0.05, 44)
+    out, out64, amx, bad = orc.gmm_fwd_block(x, codes, scale, gs, silu=False, want_f64=True,
+                                             want_acc_max=True)
+    assert bad == 0
+    q, sb, _ = orc.quantize_rows_block(x, gs)
+    qd = q.view(F8).double().numpy()
+    wd = codes.view(F8).double().numpy()
+    for m in range(M):
+        e = 0 if m < 2 else 1
+        for n in range(N):
+            acc = 0.0
+            for b, (k0, k1) in enumerate([(0, 512), (512, 1024), (1024, 1280)]):
+                d = float(np.float32(np.dot(qd[m, k0:k1], wd[e, k0:k1, n])))
+                v = acc + d * float(sb[m, b])
+                acc = float(orc.f64_to_bf16(torch.tensor([v], dtype=torch.float64)).float())
+            y = acc * float(scale[e, n])
+            assert out64[m, n].item() == y
+            assert out[m, n].view(torch.int16) == orc.f64_to_bf16(torch.tensor([y])).view(torch.int16)[0]
+
+
+def test_gmm_fwd_block_lossless_case_is_integer_matmul(orc):
+    """Every block of every row holds one 448 (on a weight row of zeros) and
+    small integers elsewhere; weights are 0 / +-1 with channel scale 1: every
+    block scale is 1, codes and block products are exact integers below 256 and
+    the bf16 accumulation is exact, so the result equals the integer matmul."""
+    M, K, N, E = 16, 1536, 12, 1
+    g = torch.Generator().manual_seed(45)
+    x = torch.zeros(M, K)
+    nz = torch.rand(M, K, generator=g) < 0.02
+    x[nz] = torch.randint(-2, 3, (int(nz.sum()),), generator=g).float()
+    for b in range(3):
+        x[:, 512 * b + 7] = 448.0
+    w = torch.randint(-1, 2, (K, N), generator=g).float()
+    for b in range(3):
+        w[512 * b + 7] = 0.0
+    codes = w.to(F8).view(torch.uint8)[None].contiguous()
+    scale = torch.ones(E, N)
+    gs = torch.tensor([M], dtype=torch.int32)
+    out, out64, _, bad = orc.gmm_fwd_block(x.to(torch.bfloat16), codes, scale, gs, silu=False,
+                                           want_f64=True)
+    assert bad == 0
+    ref = x.double() @ w.double()
+    assert ref.abs().max() < 256
+    assert torch.equal(out64, ref)
+    full, _, _ = orc.gmm_fwd(x.to(torch.bfloat16), codes, scale, gs, silu=False)
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+
+
 # ------------------------------------------------------ dSwiGLU (wo backward)
 def _autograd_dswiglu(dh64, gu):
     """Gradients of sum(dh * silu(g) * u) w.r.t. g and u, float64 autograd."""
