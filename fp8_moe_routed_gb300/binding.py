@@ -27,6 +27,7 @@ OP_GMM_SILU_FP8_FWD = 2
 OP_GMM_DLHS_FP8 = 3
 OP_TGMM_DRHS_QUANT = 4
 OP_GMM_BF16_FWD = 5
+OP_GMM_FP8_FWD_BLOCK = 7
 
 STATUS_NEGATIVE_GROUP = 0x1
 STATUS_GROUPS_EXCEED_M = 0x2
@@ -41,6 +42,7 @@ EXPORTS = [
     "fp8moe_last_cuda_error", "fp8moe_num_sms", "fp8moe_gmm_silu_fp8_fwd_noalloc",
     "fp8moe_gmm_dlhs_dswiglu_fp8", "fp8moe_gmm_dlhs_dswiglu_fp8_path",
     "fp8moe_tgmm_drhs_quant_fmt", "fp8moe_tgmm_quantize_tiles_fmt",
+    "fp8moe_gmm_fp8_fwd_block", "fp8moe_quantize_rows_block",
 ]
 
 FMT = {"e4m3": 0, "e5m2": 1}
@@ -92,6 +94,9 @@ def load(build_if_missing: bool = True):
             "fp8moe_tgmm_drhs_quant_fmt": ([P, P, I64, I64, I64, I32, P, P, P, SZ, I32, P], I32),
             "fp8moe_tgmm_quantize_tiles_fmt": ([P, P, I64, I64, I64, I32, P, P, P, P, P, I32, P],
                                                I32),
+            "fp8moe_gmm_fp8_fwd_block": ([P, I64, I64, P, P, I32, I64, P, P, P, SZ, I32, I32, P],
+                                         I32),
+            "fp8moe_quantize_rows_block": ([P, I64, I64, P, I32, I32, P, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -178,6 +183,48 @@ def gmm_fp8_fwd(lhs, codes, scale, group_sizes, out=None, workspace=None):
 def gmm_silu_fp8_fwd(lhs, codes, scale, group_sizes, out=None, workspace=None):
     """wi forward with fused SwiGLU: bf16 [M, N/2] (see fp8moe_gmm_silu_fp8_fwd)."""
     return _fwd(lhs, codes, scale, group_sizes, out, workspace, silu=True)
+
+
+def gmm_fp8_fwd_block(lhs, codes, scale, group_sizes, swiglu: bool, out=None, workspace=None,
+                      block: int = 512):
+    """Forward GMM with per-512-column block activation scales and bf16
+    accumulation across blocks (see fp8moe_gmm_fp8_fwd_block)."""
+    L = load()
+    _req(lhs, torch.bfloat16, "lhs", 2)
+    _req(codes, torch.uint8, "codes", 3)
+    _req(scale, torch.float32, "scale", 2)
+    _req(group_sizes, torch.int32, "group_sizes", 1)
+    M, K = lhs.shape
+    E, K2, N = codes.shape
+    if K2 != K or scale.shape != (E, N) or group_sizes.numel() != E:
+        raise ValueError("shape mismatch")
+    Nout = N // 2 if swiglu else N
+    if out is None:
+        out = torch.empty(M, Nout, dtype=torch.bfloat16, device=lhs.device)
+    else:
+        _req(out, torch.bfloat16, "out", 2)
+    ws, wsb = _workspace(OP_GMM_FP8_FWD_BLOCK, M, K, N, E, lhs.device, workspace)
+    _check(L.fp8moe_gmm_fp8_fwd_block(_ptr(lhs), M, K, _ptr(codes), _ptr(scale), E, N,
+                                      _ptr(group_sizes), _ptr(out), _ptr(ws), wsb, block,
+                                      1 if swiglu else 0, _stream(lhs.device)),
+           "fp8moe_gmm_fp8_fwd_block")
+    return out
+
+
+def quantize_rows_block(lhs, group_sizes, block: int = 512):
+    """Parity export of the per-block activation quantization: codes u8 [M, K]
+    and bf16-valued f32 scales [M, ceil(K / block)]."""
+    L = load()
+    _req(lhs, torch.bfloat16, "lhs", 2)
+    _req(group_sizes, torch.int32, "group_sizes", 1)
+    M, K = lhs.shape
+    nb = (K + block - 1) // block
+    q = torch.zeros(M, K, dtype=torch.uint8, device=lhs.device)
+    sb = torch.full((M, nb), float("nan"), dtype=torch.float32, device=lhs.device)
+    _check(L.fp8moe_quantize_rows_block(_ptr(lhs), M, K, _ptr(group_sizes), group_sizes.numel(),
+                                        block, _ptr(q), _ptr(sb), _stream(lhs.device)),
+           "fp8moe_quantize_rows_block")
+    return q, sb
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

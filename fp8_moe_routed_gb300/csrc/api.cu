@@ -111,6 +111,12 @@ size_t fwd_ws_bytes(int64_t M, int64_t K) {
   return round_up((size_t)M * (size_t)K, 256) + round_up((size_t)M * 4, 256);
 }
 
+constexpr int64_t kQuantBlock = 512;
+size_t fwd_block_ws_bytes(int64_t M, int64_t K) {
+  const int64_t nb = (K + kQuantBlock - 1) / kQuantBlock;
+  return round_up((size_t)M * (size_t)K, 256) + round_up((size_t)M * (size_t)nb * 4, 256);
+}
+
 struct TgmmWorkspace {
   uint8_t* qx;
   uint8_t* qd;
@@ -188,6 +194,7 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   if (e != cudaSuccess) return cuda_fail(e);
   a.e0 = 0;
   a.e1 = E;
+  a.blk = 0;
   e = fp8moe_launch_gmm_fp8_fwd(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
@@ -260,6 +267,8 @@ size_t fp8moe_workspace_size(int op, int64_t M, int64_t K, int64_t N, int32_t E)
       return fwd_ws_bytes(M, K);
     case FP8MOE_OP_TGMM_DRHS_QUANT:
       return tgmm_ws_bytes(M, K, N, E);
+    case FP8MOE_OP_GMM_FP8_FWD_BLOCK:
+      return fwd_block_ws_bytes(M, K);
     default:
       return 0;
   }
@@ -444,7 +453,87 @@ int fp8moe_gmm_bf16_fwd(const void* lhs, int64_t M, int64_t K, const void* w, in
   a.swiglu = swiglu ? 1 : 0;
   a.e0 = 0;
   a.e1 = E;
+  a.blk = 0;
   cudaError_t e = fp8moe_launch_gmm_bf16_fwd(a, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8MOE_OK;
+}
+
+int fp8moe_gmm_fp8_fwd_block(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
+                             const float* scale, int32_t E, int64_t N,
+                             const int32_t* group_sizes, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t block, int32_t swiglu,
+                             fp8moe_stream_t stream) {
+  int rc = check_common(M, K, N, E);
+  if (rc) return rc;
+  if (block != kQuantBlock || (swiglu != 0 && swiglu != 1)) return FP8MOE_EINVAL;
+  if (swiglu && (N % 32 != 0)) return FP8MOE_EALIGN;
+  if (M == 0) return FP8MOE_OK;
+  if (!workspace) return FP8MOE_EWORKSPACE;
+  if (!lhs || !codes || !scale || !group_sizes || !out) return FP8MOE_EINVAL;
+  if (!aligned16(lhs) || !aligned16(codes) || !aligned16(scale) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+    return FP8MOE_EALIGN;
+  if (workspace_bytes < fwd_block_ws_bytes(M, K)) return FP8MOE_EWORKSPACE;
+  int sms = 0;
+  rc = device_init(&sms);
+  if (rc) return rc;
+  uint8_t* q = static_cast<uint8_t*>(workspace);
+  float* sb = reinterpret_cast<float*>(q + round_up((size_t)M * (size_t)K, 256));
+  cudaError_t e = fp8moe_launch_quantize_rows_block(lhs, M, (int)K, group_sizes, E, q, sb, sms, 1,
+                                                    stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  GmmFwdArgs a;
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
+    const uint64_t st[1] = {(uint64_t)K};
+    const uint32_t box[2] = {128, 128};
+    rc = make_tmap(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, dims, st, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)N, (uint64_t)N * (uint64_t)K};
+    const uint32_t box[3] = {128, 128, 1};
+    rc = make_tmap(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, codes, dims, st, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  a.sx = sb;
+  a.scale = scale;
+  a.gs = group_sizes;
+  a.out = out;
+  a.M = M;
+  a.K = (int)K;
+  a.N = (int)N;
+  a.E = E;
+  a.swiglu = swiglu;
+  a.e0 = 0;
+  a.e1 = E;
+  a.blk = 1;
+  e = fp8moe_launch_gmm_fp8_fwd(a, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8MOE_OK;
+}
+
+int fp8moe_quantize_rows_block(const void* lhs, int64_t M, int64_t K, const int32_t* group_sizes,
+                               int32_t E, int32_t block, uint8_t* q, float* sb,
+                               fp8moe_stream_t stream) {
+  int rc = check_common(M, K, 16, E);
+  if (rc) return rc;
+  if (block != kQuantBlock) return FP8MOE_EINVAL;
+  if (M == 0) return FP8MOE_OK;
+  if (!lhs || !group_sizes || !q || !sb) return FP8MOE_EINVAL;
+  if (!aligned16(lhs) || !aligned16(q) || (reinterpret_cast<uintptr_t>(sb) & 3u) ||
+      (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+    return FP8MOE_EALIGN;
+  int sms = 0;
+  rc = device_init(&sms);
+  if (rc) return rc;
+  cudaError_t e = fp8moe_launch_quantize_rows_block(lhs, M, (int)K, group_sizes, E, q, sb, sms, 1,
+                                                    stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
 }

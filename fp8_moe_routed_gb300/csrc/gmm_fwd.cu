@@ -91,9 +91,36 @@ __device__ __forceinline__ Unit decode_unit(const Smem& s, int E, int nt, int u,
   return r;
 }
 
+// Block mode (BLK, FP8 only): per-512-column block activation scales sx [M, nblk]
+// and bf16 accumulation across blocks (the ops-level lhs_quant_block_size = 512
+// option of "MoE: native FP8 QAT for routed-expert GMMs", Implementation). The
+// MMA starts a fresh TMEM accumulator every 512 K columns (four 128-column
+// steps) and alternates the two accumulators block by block; the epilogue warps
+// fold each block into a bf16 register accumulator, acc = bf16(acc + P * s_b),
+// and apply the channel scales (and SwiGLU) once at the end of the unit.
+constexpr int kBlkSteps = 4;      // 128-column K steps per 512-column block
+
+// 16 bf16 values (8 words) of one output row, 16-byte stores; columns past
+// Nout are skipped.
+__device__ __forceinline__ void store_row_chunk(const uint32_t* o, bool row_ok,
+                                                __nv_bfloat16* __restrict__ orow, int col0,
+                                                int Nout) {
+  if (!row_ok) return;
+  if (col0 + 32 <= Nout) {
+    uint4* dst = reinterpret_cast<uint4*>(orow + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
+#pragma unroll
+    for (int q = 0; q < 32; ++q)
+      if (col0 + q < Nout) dst[col0 + q] = (uint16_t)(o[q / 2] >> (16 * (q & 1)));
+  }
+}
+
 // FP8: a 128-byte swizzle row holds 128 K values of A (or 128 N values of B);
 // BF16: 64.
-template <bool FP8, bool SWIGLU>
+template <bool FP8, bool SWIGLU, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1)
 gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const float* __restrict__ sx, const float* __restrict__ scale,
@@ -217,10 +244,17 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t aph = 0;
       bool ok = true;
       for (int u = cluster; u < total && ok; u += nclusters) {
-        if (!mbar_wait_cluster(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * kBN);
+        if (!BLK) {
+          if (!mbar_wait_cluster(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
+          tc_fence_after();
+        }
+        uint32_t d = tmem + (uint32_t)(acc * kBN);
         for (int kb = 0; kb < nkb; ++kb) {
+          if (BLK && kb % kBlkSteps == 0) {   // a fresh accumulator per 512-column block
+            if (!mbar_wait_cluster(&s.tempty[acc], aph ^ 1, kWhereMma)) { ok = false; break; }
+            tc_fence_after();
+            d = tmem + (uint32_t)(acc * kBN);
+          }
           if (!mbar_wait_cluster(&s.full[st], ph, kWhereMma)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(tiles + st * kStageBytes);
@@ -229,16 +263,24 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = make_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
             const uint64_t bd = make_desc(b_addr + kk * kBStep, kBLbo, 1024, kSwizzle128B);
-            if (FP8) mma_f8f6f4_pair(d, ad, bd, idesc, (kb | kk) != 0);
-            else mma_f16_pair(d, ad, bd, idesc, (kb | kk) != 0);
+            const bool accumulate = BLK ? ((kb % kBlkSteps) | kk) != 0 : (kb | kk) != 0;
+            if (FP8) mma_f8f6f4_pair(d, ad, bd, idesc, accumulate);
+            else mma_f16_pair(d, ad, bd, idesc, accumulate);
           }
           mma_commit_pair(&s.empty[st]);
           if (++st == kStages) { st = 0; ph ^= 1; }
+          if (BLK && (kb % kBlkSteps == kBlkSteps - 1 || kb == nkb - 1)) {
+            mma_commit_pair(&s.tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+          }
         }
         if (!ok) break;
-        mma_commit_pair(&s.tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1;
+        if (!BLK) {
+          mma_commit_pair(&s.tfull[acc]);
+          acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        }
       }
       // all MMAs complete (in both CTAs' TMEM) before TMEM may be released
       mma_commit_pair(&s.drain);
@@ -277,6 +319,79 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       named_bar_sync(1, 128);
       const bool row_ok = r < t.rows;
       const int64_t row = (int64_t)t.row0 + r;
+      if (BLK) {
+        // ---- block mode: fold every block's accumulator into bf16 registers
+        uint32_t accb[kBN / 2];           // bf16 pairs of columns (2i, 2i + 1)
+#pragma unroll
+        for (int i = 0; i < kBN / 2; ++i) accb[i] = 0u;
+        const int nblk = (nkb + kBlkSteps - 1) / kBlkSteps;
+        const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+        for (int b = 0; b < nblk; ++b) {
+          const float sbk = row_ok ? __ldg(sx + row * nblk + b) : 0.0f;
+          if (!failed && !mbar_wait_warp_cluster(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
+          if (!failed) {
+            tc_fence_after();
+            if (t.rows > 0) {
+              const uint32_t tbase = trow + (uint32_t)(acc * kBN);
+#pragma unroll
+              for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tbase + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  float f0 = bf16lo_to_f32(accb[c * 16 + i]), f1 = bf16hi_to_f32(accb[c * 16 + i]);
+                  f0 = __fmaf_rn(__uint_as_float(v[2 * i]), sbk, f0);
+                  f1 = __fmaf_rn(__uint_as_float(v[2 * i + 1]), sbk, f1);
+                  accb[c * 16 + i] = f32x2_to_bf16x2(f0, f1);
+                }
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[acc]), 0));
+          }
+          acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        }
+        if (!failed && t.rows > 0) {
+          __nv_bfloat16* orow = out + row * Nout;
+          if (SWIGLU) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                float y[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint32_t gw = accb[(c * 32 + i) / 2], uw = accb[(128 + c * 32 + i) / 2];
+                  const float gg = __fmul_rn(h ? bf16hi_to_f32(gw) : bf16lo_to_f32(gw),
+                                             s.sw[sb][c * 32 + i + h]);
+                  const float uu = __fmul_rn(h ? bf16hi_to_f32(uw) : bf16lo_to_f32(uw),
+                                             s.sw[sb][128 + c * 32 + i + h]);
+                  y[h] = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg))), uu);
+                }
+                o[i / 2] = f32x2_to_bf16x2(y[0], y[1]);
+              }
+              store_row_chunk(o, row_ok, orow, t.j * 128 + c * 32, Nout);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+              uint32_t o[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                o[i] = f32x2_to_bf16x2(__fmul_rn(bf16lo_to_f32(accb[c * 16 + i]), s.sw[sb][c * 32 + 2 * i]),
+                                       __fmul_rn(bf16hi_to_f32(accb[c * 16 + i]),
+                                                 s.sw[sb][c * 32 + 2 * i + 1]));
+              store_row_chunk(o, row_ok, orow, t.j * kBN + c * 32, Nout);
+            }
+          }
+        }
+        sb ^= 1;
+        continue;
+      }
       const float sxr = (FP8 && row_ok) ? __ldg(sx + row) : 1.0f;
       if (!failed && !mbar_wait_warp_cluster(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
       if (failed) {
@@ -363,9 +478,9 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <bool FP8, bool SWIGLU>
+template <bool FP8, bool SWIGLU, bool BLK>
 cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gmm_fwd_kernel<FP8, SWIGLU>;
+  auto kern = gmm_fwd_kernel<FP8, SWIGLU, BLK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -393,11 +508,13 @@ cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
 FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_gmm_fwd)
 
 cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
-  return a.swiglu ? fp8moe::fwd::launch<true, true>(a, num_sms, s)
-                  : fp8moe::fwd::launch<true, false>(a, num_sms, s);
+  using namespace fp8moe::fwd;
+  if (a.blk)
+    return a.swiglu ? launch<true, true, true>(a, num_sms, s) : launch<true, false, true>(a, num_sms, s);
+  return a.swiglu ? launch<true, true, false>(a, num_sms, s) : launch<true, false, false>(a, num_sms, s);
 }
 
 cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
-  return a.swiglu ? fp8moe::fwd::launch<false, true>(a, num_sms, s)
-                  : fp8moe::fwd::launch<false, false>(a, num_sms, s);
+  using namespace fp8moe::fwd;
+  return a.swiglu ? launch<false, true, false>(a, num_sms, s) : launch<false, false, false>(a, num_sms, s);
 }

@@ -10,6 +10,10 @@
 cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const int32_t* gs,
                                         int E, int e0, int e1, uint8_t* q, float* sx, int num_sms,
                                         int ctas_per_sm, int report, cudaStream_t s);
+// Per-512-column block quantization: codes q [M, K], bf16-valued scales sb [M, ceil(K/512)].
+cudaError_t fp8moe_launch_quantize_rows_block(const void* lhs, int64_t M, int K, const int32_t* gs,
+                                              int E, uint8_t* q, float* sb, int num_sms, int report,
+                                              cudaStream_t s);
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
@@ -29,6 +33,8 @@ struct GmmFwdArgs {
   int64_t M;
   int K, N, E, swiglu;
   int e0, e1;             // only the units of experts [e0, e1)
+  int blk;                // 1: sx holds per-512-column block scales [M, ceil(K/512)] and the
+                          //    accumulation across blocks is bf16 (FP8 arm only)
 };
 cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);
 cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);

@@ -209,6 +209,62 @@ __global__ void __launch_bounds__(kQThreads) quantize_rows_stream_kernel(
   }
 }
 
+// ------------------------------------------- per-512-column block quantization
+// The ops-level option of "MoE: native FP8 QAT for routed-expert GMMs"
+// (Implementation, lhs_quant_block_size = 512): one bf16 scale per row and
+// 512-column block, s = bf16(max(amax over the block, 1e-12) / 448) (IEEE f32
+// division, then round to nearest even to bf16), codes = e4m3(x / s). One warp
+// per (row, block): 64 16-byte pieces, two per lane; the grid strides over the
+// (row, block) pairs of rows < T.
+constexpr int kBlockCols = 512;
+
+__global__ void __launch_bounds__(kQThreads) quantize_rows_block_kernel(
+    const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
+    int E, uint8_t* __restrict__ q, float* __restrict__ sb, int report) {
+  __shared__ int32_t s_lo, s_hi;
+  group_row_range_warp0(gs, E, M, 0, E, &s_lo, &s_hi, report && blockIdx.x == 0);
+  __syncthreads();
+  const int64_t T = s_hi;
+  const int lane = threadIdx.x & 31;
+  const int nb = (K + kBlockCols - 1) / kBlockCols;
+  const int64_t nwarps = (int64_t)gridDim.x * (kQThreads / 32);
+  for (int64_t w = (int64_t)blockIdx.x * (kQThreads / 32) + (threadIdx.x >> 5); w < T * nb;
+       w += nwarps) {
+    const int64_t m = w / nb;
+    const int b = (int)(w - m * nb);
+    const int k0 = b * kBlockCols;
+    const int nchunk = (min(K, k0 + kBlockCols) - k0) >> 3;   // 16-byte pieces, K % 16 == 0
+    const uint4* src = reinterpret_cast<const uint4*>(lhs + m * K + k0);
+    uint4 v[2];
+    uint32_t amax2 = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = lane + 32 * i;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < nchunk) {
+        v[i] = __ldg(src + c);
+        amax2 = bf16x2_absmax(amax2, v[i].x);
+        amax2 = bf16x2_absmax(amax2, v[i].y);
+        amax2 = bf16x2_absmax(amax2, v[i].z);
+        amax2 = bf16x2_absmax(amax2, v[i].w);
+      }
+    }
+    float amax = bf16x2_hmax_to_f32(amax2);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = __bfloat162float(__float2bfloat16_rn(__fdiv_rn(fmaxf(amax, kEps), kE4m3Max)));
+    float rl, rh;
+    bracket(s, rl, rh);
+    uint2* dst = reinterpret_cast<uint2*>(q + m * K + k0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nchunk) dst[c] = quant8(v[i], s, rl, rh);
+    }
+    if (lane == 0) sb[m * nb + b] = s;
+  }
+}
+
 // ------------------------------------------------------------------------ a7
 // Segment table: nseg[e] = number of 128-row tiles touched by group e, seg_base =
 // exclusive prefix (segments numbered expert by expert, tiles ascending).
@@ -382,6 +438,20 @@ cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const
     quantize_rows_kernel<4><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
   else
     quantize_rows_stream_kernel<<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
+  return cudaGetLastError();
+}
+
+cudaError_t fp8moe_launch_quantize_rows_block(const void* lhs, int64_t M, int K, const int32_t* gs,
+                                              int E, uint8_t* q, float* sb, int num_sms, int report,
+                                              cudaStream_t s) {
+  using namespace fp8moe;
+  const int64_t warps = M * ((K + kBlockCols - 1) / kBlockCols);
+  const int64_t need = (warps + kQThreads / 32 - 1) / (kQThreads / 32);
+  const int64_t cap = (int64_t)num_sms * 8;
+  int grid = (int)(need < cap ? need : cap);
+  if (grid < 1) grid = 1;
+  quantize_rows_block_kernel<<<grid, kQThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(lhs), M,
+                                                        K, gs, E, q, sb, report);
   return cudaGetLastError();
 }
 

@@ -61,7 +61,8 @@ enum {
   FP8MOE_OP_GMM_DLHS_FP8 = 3,
   FP8MOE_OP_TGMM_DRHS_QUANT = 4,
   FP8MOE_OP_GMM_BF16_FWD = 5,
-  FP8MOE_OP_DEQUANTIZE = 6
+  FP8MOE_OP_DEQUANTIZE = 6,
+  FP8MOE_OP_GMM_FP8_FWD_BLOCK = 7
 };
 
 /* fp8 formats of the tgmm's dout (gradient) operand -- [DQ] What: the
@@ -186,6 +187,29 @@ int fp8moe_dequantize_fp8_codes(const uint8_t* codes, const float* scale, int32_
 int fp8moe_gmm_bf16_fwd(const void* lhs, int64_t M, int64_t K, const void* w, int32_t E,
                         int64_t N, const int32_t* group_sizes, int32_t swiglu, void* out,
                         fp8moe_stream_t stream);
+
+/* Forward GMM with per-block activation quantization -- [NQ] Implementation:
+ * the ops-level lhs_quant_block_size = 512 option (the pages' earlier default;
+ * the production forward is fp8moe_gmm_fp8_fwd's full-K f32 scale).  Per row m
+ * and block b of 512 columns (the last one may be shorter):
+ *   sb[m,b] = bf16( max(max_{k in b} |lhs[m,k]|, 1e-12) / 448 ),  q = e4m3(lhs / sb)
+ *   acc = 0 (bf16); for each block b:  acc = bf16( acc + sb[m,b] * P_b[m,n] ),
+ *     P_b = the f32 product of the block's codes,  sum_{k in b} q[m,k] * codes[e,k,n]
+ *   out[m,n] = bf16( acc * scale[e,n] ), or with swiglu = 1 the SwiGLU of the
+ *   gate | up halves as fp8moe_gmm_silu_fp8_fwd (out [M, N/2]).
+ * block must be 512 (FP8MOE_EINVAL otherwise).  Workspace:
+ * FP8MOE_OP_GMM_FP8_FWD_BLOCK (codes and block scales).  Rows >= T untouched. */
+int fp8moe_gmm_fp8_fwd_block(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
+                             const float* scale, int32_t E, int64_t N,
+                             const int32_t* group_sizes, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t block, int32_t swiglu,
+                             fp8moe_stream_t stream);
+
+/* Parity export of the block quantization above: q u8 [M, K] and the
+ * bf16-valued f32 scales sb [M, ceil(K/512)] for rows < T. */
+int fp8moe_quantize_rows_block(const void* lhs, int64_t M, int64_t K, const int32_t* group_sizes,
+                               int32_t E, int32_t block, uint8_t* q, float* sb,
+                               fp8moe_stream_t stream);
 
 /* Parity export of the forward activation quantization: q u8 [M, K] and
  * sx f32 [M] for rows < T (rows >= T untouched). */

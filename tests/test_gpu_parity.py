@@ -7,7 +7,7 @@ import torch
 
 from fp8_moe_routed_gb300 import binding as fb
 from fp8_moe_routed_gb300 import workloads as W
-from parity_util import bits16, check_bf16, check_f32_rel
+from parity_util import bf16_ulp, bits16, check_bf16, check_f32_rel
 
 pytestmark = pytest.mark.gpu
 
@@ -364,6 +364,82 @@ def test_tgmm_rejects_unknown_dout_format():
     rc = L.fp8moe_tgmm_drhs_quant_fmt(fb._ptr(x), fb._ptr(d), 128, 64, 64, 1, fb._ptr(gs),
                                       fb._ptr(out), fb._ptr(ws), ws.numel(), 2, fb._stream(x.device))
     assert rc == -1
+
+
+# ---------------------------------- per-512 block quantization (NEXT-3)
+BLOCK_CASES = [
+    (512, 1024, 256, 4, "tiny"),
+    (1024, 1280, 384, 3, [300, 0, 500]),     # K = 1280: partial last block; tail garbage
+    (640, 7168, 512, 2, [0, 600]),            # 14 blocks, first expert empty
+]
+
+
+def _block_case(M, K, E, gs, seed):
+    if gs == "tiny":
+        gs = W.group_sizes("tiny", seed=seed, M=M, E=E)
+    gs = torch.tensor(gs, dtype=torch.int32) if isinstance(gs, list) else gs
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=K + seed), T)
+    return gs, T, x
+
+
+@pytest.mark.parametrize("M,K,N,E,gs", BLOCK_CASES)
+def test_quantize_rows_block_bit_exact(orc, M, K, N, E, gs):
+    gs, T, x = _block_case(M, K, E, gs, 1)
+    q, sb = fb.quantize_rows_block(*cuda(x, gs))
+    rq, rsb, bad = orc.quantize_rows_block(x, gs)
+    assert bad == 0
+    assert torch.equal(sb.cpu()[:T], rsb[:T]) and torch.equal(q.cpu()[:T], rq[:T])
+
+
+@pytest.mark.parametrize("M,K,N,E,gs", BLOCK_CASES)
+def test_gmm_fwd_block_vs_oracle(orc, M, K, N, E, gs):
+    """Tolerance from the arithmetic: GPU and oracle take the same bf16
+    rounding steps; the f32 block product (summation order) and the fused
+    multiply-add before the bf16 rounding can flip a step by one bf16 ulp of the
+    running sum, so |gpu - ref| <= nblk * ulp(max |acc|) * |sw| + 1 ulp(ref);
+    and almost every element is bit-identical."""
+    gs, T, x = _block_case(M, K, E, gs, 2)
+    codes, scale = W.fp8_weights(E, K, N, 0.05, seed=E + 7)
+    out = fb.gmm_fp8_fwd_block(*cuda(x, codes, scale, gs), False)
+    ref, _, amx, bad = orc.gmm_fwd_block(x, codes, scale, gs, silu=False, want_acc_max=True)
+    assert bad == 0
+    nblk = (K + 511) // 512
+    g, r = out.cpu()[:T].double(), ref[:T].double()
+    assert torch.isfinite(g).all()
+    sw = torch.zeros(T, N, dtype=torch.float64)
+    off = 0
+    for e, n in enumerate(gs.tolist()):
+        sw[off:off + n] = scale[e].double()
+        off += n
+    bound = nblk * bf16_ulp(amx[:T]) * sw.abs() + bf16_ulp(r)
+    assert ((g - r).abs() <= bound).all()
+    same = (out.cpu()[:T].view(torch.int16) == ref[:T].view(torch.int16)).float().mean().item()
+    assert same > 0.95, same
+
+
+@pytest.mark.parametrize("M,K,N,E,gs", BLOCK_CASES[1:])
+def test_gmm_fwd_block_swiglu_vs_oracle(orc, M, K, N, E, gs):
+    gs, T, x = _block_case(M, K, E, gs, 3)
+    codes, scale = W.fp8_weights(E, K, N, 0.05, seed=E + 8)
+    out = fb.gmm_fp8_fwd_block(*cuda(x, codes, scale, gs), True)
+    ref, _, _, bad = orc.gmm_fwd_block(x, codes, scale, gs, silu=True)
+    assert bad == 0
+    g, r = out.cpu()[:T].double(), ref[:T].double()
+    assert torch.isfinite(g).all()
+    same = (out.cpu()[:T].view(torch.int16) == ref[:T].view(torch.int16)).float().mean().item()
+    assert same > 0.9, same
+    rms = r.pow(2).mean().sqrt().item()
+    assert (g - r).abs().max().item() <= 0.05 * rms
+
+
+def test_gmm_fwd_block_rejects_other_block_sizes():
+    x = torch.zeros(128, 512, dtype=torch.bfloat16, device=DEV)
+    codes = torch.zeros(1, 512, 64, dtype=torch.uint8, device=DEV)
+    scale = torch.ones(1, 64, device=DEV)
+    gs = torch.tensor([128], dtype=torch.int32, device=DEV)
+    with pytest.raises(fb.Fp8MoeError):
+        fb.gmm_fp8_fwd_block(x, codes, scale, gs, False, block=256)
 
 
 # --------------------------------------------------------- BF16 comparison
