@@ -21,7 +21,8 @@
 //                bf16, write the [256 x 64] bf16 B operand in the K-major
 //                128-byte-swizzle layout the tensor core reads (2-deep ring).
 //   warp 1       tcgen05.mma kind::f16 (M=128, N=256, K=16) into TMEM.
-//   warps 2..5   epilogue: TMEM -> bf16 -> row-masked stores. TMEM holds two
+//   warps 2..5,  epilogue: TMEM -> bf16 -> row-masked stores, two warps per
+//   14..17       TMEM lane quarter, each one half of the columns. TMEM holds two
 //                accumulators: the two m tiles of a streaming unit, or (cached)
 //                consecutive m tiles so that the epilogue overlaps the MMAs.
 // dSwiGLU variant (DSW): the wo dLHS of "gmm_dswiglu_fp8" ([NQ] Implementation)
@@ -56,7 +57,12 @@ constexpr int kABytes = kBM * kBK * 2;   // 16 KB dout tile
 constexpr int kCBytes = kBN * kBK;       // 16 KB codes tile
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB bf16 operand
 constexpr int kDqWarps = 8;
-constexpr int kThreads = (6 + kDqWarps) * 32;   // 448
+constexpr int kEpiWarps = 8;                    // two per TMEM lane quarter
+constexpr int kThreads = (2 + kEpiWarps + kDqWarps) * 32;   // 576
+// Registers are budgeted per SM sub-partition: 18 warps put 5 on two of them,
+// so a thread may hold 16384 / (5 * 32) -> 96 registers; launch bounds of 640
+// threads give the compiler that cap.
+constexpr int kRegBudgetThreads = 640;
 constexpr int kTmemCols = 512;
 constexpr int kMaxCachedSteps = 4;       // cached variant: N <= 256
 constexpr int kCachedRun = 8;            // m tiles per cached work unit
@@ -169,9 +175,10 @@ __device__ __forceinline__ void load_scales16(const float* __restrict__ scale, i
 
 // Epilogue of one finished accumulator: 128 rows x 256 columns f32 -> bf16.
 __device__ __forceinline__ void store_tile(uint32_t tbase, int r, bool row_ok,
-                                           __nv_bfloat16* __restrict__ orow, int col_base, int K) {
+                                           __nv_bfloat16* __restrict__ orow, int col_base, int K,
+                                           int nchunks) {
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < nchunks; ++c) {
     uint32_t v[32];
     tmem_ld32(tbase + c * 32, v);
     tmem_ld_wait();
@@ -223,9 +230,9 @@ __device__ __forceinline__ void dswiglu8(const uint4& gw, const uint4& uw, const
 __device__ __forceinline__ void store_tile_dswiglu(uint32_t tbase, bool row_ok,
                                                    const __nv_bfloat16* __restrict__ gurow,
                                                    __nv_bfloat16* __restrict__ orow, int col_base,
-                                                   int F) {
+                                                   int F, int nchunks) {
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < nchunks; ++c) {
     uint32_t v[32];
     tmem_ld32(tbase + c * 32, v);
     tmem_ld_wait();
@@ -253,7 +260,7 @@ __device__ __forceinline__ void store_tile_dswiglu(uint32_t tbase, bool row_ok,
 }
 
 template <bool CACHED, bool DSW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kRegBudgetThreads, 1)
 gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                 const float* __restrict__ scale, const int32_t* __restrict__ gs,
                 const __nv_bfloat16* __restrict__ gu, __nv_bfloat16* __restrict__ dlhs, int64_t M,
@@ -320,7 +327,7 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mbar_init(&s.c_empty, kDqWarps);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 4);   // one elected lane per epilogue warp
+        mbar_init(&s.tempty[i], kEpiWarps);   // one elected lane per epilogue warp
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -453,10 +460,13 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       mma_commit(&s.drain);
       mbar_wait(&s.drain, 0, kWhereDrain);
     }
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= 6 + kDqWarps) {
     // =============================== epilogue =============================
+    // two warps per TMEM lane quarter: each drains one half of the 256 columns
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    const int half = warp >= 6 + kDqWarps ? 1 : 0;
+    constexpr int kHalfCols = kBN / 2;
     int acc = 0;
     uint32_t aph = 0;
     bool ok = true;
@@ -476,11 +486,14 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           tc_fence_after();
           col_acc = acc;
         }
-        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(col_acc * kBN);
+        const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(col_acc * kBN + half * kHalfCols);
+        const int col_base = t.j * kBN + half * kHalfCols;
         if (DSW)
-          store_tile_dswiglu(tbase, row_ok, gu + row * 2 * K, dlhs + row * 2 * K, t.j * kBN, K);
+          store_tile_dswiglu(tbase, row_ok, gu + row * 2 * K, dlhs + row * 2 * K, col_base, K,
+                             kHalfCols / 32);
         else
-          store_tile(tbase, r, row_ok, dlhs + row * K, t.j * kBN, K);
+          store_tile(tbase, r, row_ok, dlhs + row * K, col_base, K, kHalfCols / 32);
         if (CACHED) {
           tc_fence_before();
           __syncwarp();
