@@ -3,9 +3,11 @@
 // routed-expert GMMs", Implementation: dequantize_fp8_codes, bit-identical to
 // the weight dequantization of the fake-QAT path).
 //
-// HBM-bound: 1 byte read + 2 bytes written per element. Each thread converts 16
-// codes (one 16-byte load, two 16-byte stores); the grid is a multiple of the SM
-// count and strides over the tensor.
+// HBM-bound: 1 byte read + 2 bytes written per element. A CTA takes four whole
+// rows of [E*K, N] per step (grid-stride over row blocks); each thread converts
+// the same 16-code vector of the four rows (four loads in flight) and writes each vector's
+// 32 output bytes with one 32-byte store (two 16-byte stores when the output is
+// only 16-byte aligned), so a warp writes whole lines.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -14,36 +16,63 @@
 
 namespace fp8moe {
 
-__global__ void __launch_bounds__(256) dequantize_kernel(const uint8_t* __restrict__ codes,
-                                                         const float* __restrict__ scale, int64_t K,
-                                                         int64_t N, int64_t nvec,
-                                                         uint4* __restrict__ out) {
+constexpr int kDqThreads = 256;
+constexpr int kRows = 4;
+
+__device__ __forceinline__ void dequant16(uint4 c, const float* __restrict__ srow, int64_t n0,
+                                          uint32_t (&o)[8]) {
+  const float4* sp = reinterpret_cast<const float4*>(srow + n0);
+  float sc[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = __ldg(sp + i);
+    sc[4 * i] = f.x; sc[4 * i + 1] = f.y; sc[4 * i + 2] = f.z; sc[4 * i + 3] = f.w;
+  }
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float f0, f1, f2, f3;
+    half2_to_f32(e4m3x2_to_f16x2((uint16_t)(cw[i] & 0xFFFFu)), f0, f1);
+    half2_to_f32(e4m3x2_to_f16x2((uint16_t)(cw[i] >> 16)), f2, f3);
+    o[2 * i] = f32x2_to_bf16x2(__fmul_rn(f0, sc[4 * i]), __fmul_rn(f1, sc[4 * i + 1]));
+    o[2 * i + 1] = f32x2_to_bf16x2(__fmul_rn(f2, sc[4 * i + 2]), __fmul_rn(f3, sc[4 * i + 3]));
+  }
+}
+
+__device__ __forceinline__ void store32(uint4* dst, const uint32_t (&o)[8], bool v32) {
+  if (v32) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(o[0]),
+                 "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
+  } else {
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+__global__ void __launch_bounds__(kDqThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                                const float* __restrict__ scale,
+                                                                int64_t rows, int64_t K, int64_t N,
+                                                                uint4* __restrict__ out) {
   const int64_t vpr = N >> 4;   // 16-code vectors per row (N % 16 == 0)
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
-       v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = v / vpr;            // row of [E*K, N]
-    const int64_t n0 = (v - row * vpr) << 4;
-    const int64_t e = row / K;
-    const uint4 c = __ldg(reinterpret_cast<const uint4*>(codes) + v);
-    const float4* sp = reinterpret_cast<const float4*>(scale + e * N + n0);
-    float sc[16];
+  const bool v32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  // kRows rows per CTA step: every thread has kRows loads in flight
+  for (int64_t r0 = (int64_t)blockIdx.x * kRows; r0 < rows; r0 += (int64_t)gridDim.x * kRows) {
+    for (int64_t v = threadIdx.x; v < vpr; v += kDqThreads) {
+      uint4 c[kRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float4 f = __ldg(sp + i);
-      sc[4 * i] = f.x; sc[4 * i + 1] = f.y; sc[4 * i + 2] = f.z; sc[4 * i + 3] = f.w;
-    }
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    uint32_t o[8];
+      for (int i = 0; i < kRows; ++i)
+        c[i] = r0 + i < rows ? __ldg(reinterpret_cast<const uint4*>(codes + (r0 + i) * N) + v)
+                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float f0, f1, f2, f3;
-      half2_to_f32(e4m3x2_to_f16x2((uint16_t)(cw[i] & 0xFFFFu)), f0, f1);
-      half2_to_f32(e4m3x2_to_f16x2((uint16_t)(cw[i] >> 16)), f2, f3);
-      o[2 * i] = f32x2_to_bf16x2(__fmul_rn(f0, sc[4 * i]), __fmul_rn(f1, sc[4 * i + 1]));
-      o[2 * i + 1] = f32x2_to_bf16x2(__fmul_rn(f2, sc[4 * i + 2]), __fmul_rn(f3, sc[4 * i + 3]));
+      for (int i = 0; i < kRows; ++i) {
+        if (r0 + i < rows) {
+          uint32_t o[8];
+          dequant16(c[i], scale + ((r0 + i) / K) * N, v << 4, o);
+          store32(out + (r0 + i) * (N >> 3) + 2 * v, o, v32);
+        }
+      }
     }
-    out[2 * v] = make_uint4(o[0], o[1], o[2], o[3]);
-    out[2 * v + 1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -53,12 +82,12 @@ FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_dequant)
 
 cudaError_t fp8moe_launch_dequantize(const uint8_t* codes, const float* scale, int E, int64_t K,
                                      int64_t N, void* out, int num_sms, cudaStream_t s) {
-  const int64_t nvec = (int64_t)E * K * N / 16;
-  int64_t blocks = (nvec + 255) / 256;
-  int64_t cap = (int64_t)num_sms * 8;
+  const int64_t rows = (int64_t)E * K;
+  const int64_t blocks = (rows + fp8moe::kRows - 1) / fp8moe::kRows;
+  const int64_t cap = (int64_t)num_sms * 8;   // 8 CTAs of 256 threads per SM
   int grid = (int)(blocks < cap ? blocks : cap);
   if (grid < 1) grid = 1;
-  fp8moe::dequantize_kernel<<<grid, 256, 0, s>>>(codes, scale, K, N, nvec,
-                                                 static_cast<uint4*>(out));
+  fp8moe::dequantize_kernel<<<grid, fp8moe::kDqThreads, 0, s>>>(codes, scale, rows, K, N,
+                                                                static_cast<uint4*>(out));
   return cudaGetLastError();
 }
