@@ -42,7 +42,7 @@ EXPORTS = [
     "fp8moe_last_cuda_error", "fp8moe_num_sms", "fp8moe_gmm_silu_fp8_fwd_noalloc",
     "fp8moe_gmm_dlhs_dswiglu_fp8", "fp8moe_gmm_dlhs_dswiglu_fp8_path",
     "fp8moe_tgmm_drhs_quant_fmt", "fp8moe_tgmm_quantize_tiles_fmt",
-    "fp8moe_gmm_fp8_fwd_block", "fp8moe_quantize_rows_block",
+    "fp8moe_gmm_fp8_fwd_block", "fp8moe_quantize_rows_block", "fp8moe_selftest_wait_timeout",
 ]
 
 FMT = {"e4m3": 0, "e5m2": 1}
@@ -97,6 +97,7 @@ def load(build_if_missing: bool = True):
             "fp8moe_gmm_fp8_fwd_block": ([P, I64, I64, P, P, I32, I64, P, P, P, SZ, I32, I32, P],
                                          I32),
             "fp8moe_quantize_rows_block": ([P, I64, I64, P, I32, I32, P, P, P], I32),
+            "fp8moe_selftest_wait_timeout": ([ctypes.c_uint32, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -405,6 +406,12 @@ def tgmm_quantize_tiles(lhs, dout, group_sizes, dout_fmt: str = "e4m3"):
                                             _stream(dev)),
            "fp8moe_tgmm_quantize_tiles")
     return qx, sx, qd, sd
+
+
+def selftest_wait_timeout(limit_us: int, device=None) -> None:
+    """Enqueue the bounded-wait failure self-test (see fp8moe_selftest_wait_timeout)."""
+    _check(load().fp8moe_selftest_wait_timeout(int(limit_us), _stream(device)),
+           "fp8moe_selftest_wait_timeout")
 
 
 def read_status(device=None) -> int:

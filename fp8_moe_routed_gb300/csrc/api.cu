@@ -582,12 +582,22 @@ int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M,
                             dout_fmt);
 }
 
+int fp8moe_selftest_wait_timeout(uint32_t limit_us, fp8moe_stream_t stream) {
+  if (limit_us == 0 || limit_us > 2000000u) return FP8MOE_EINVAL;
+  int sms = 0;
+  int rc = device_init(&sms);
+  if (rc) return rc;
+  cudaError_t e = fp8moe_launch_selftest_wait((uint64_t)limit_us * 1000u, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8MOE_OK;
+}
+
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags) {
   if (!flags) return FP8MOE_EINVAL;
   uint32_t v = 0;
   uint32_t (*takes[])(cudaStream_t) = {fp8moe_status_take_quant, fp8moe_status_take_dequant,
                                        fp8moe_status_take_gmm_fwd, fp8moe_status_take_dlhs,
-                                       fp8moe_status_take_tgmm};
+                                       fp8moe_status_take_tgmm, fp8moe_status_take_selftest};
   for (auto take : takes) {
     uint32_t x = take(stream);
     if (x == 0xFFFFFFFFu) return cuda_fail(cudaGetLastError());

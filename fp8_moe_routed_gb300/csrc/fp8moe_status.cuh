@@ -20,6 +20,7 @@ constexpr uint32_t kWhereMma = 2u << 8;
 constexpr uint32_t kWhereEpilogue = 3u << 8;
 constexpr uint32_t kWhereDequant = 4u << 8;
 constexpr uint32_t kWhereDrain = 5u << 8;
+constexpr uint32_t kWhereSelftest = 6u << 8;
 
 static __device__ uint32_t g_status_word;
 

@@ -73,3 +73,8 @@ uint32_t fp8moe_status_take_dequant(cudaStream_t s);
 uint32_t fp8moe_status_take_gmm_fwd(cudaStream_t s);
 uint32_t fp8moe_status_take_dlhs(cudaStream_t s);
 uint32_t fp8moe_status_take_tgmm(cudaStream_t s);
+uint32_t fp8moe_status_take_selftest(cudaStream_t s);
+
+// One thread waits on an mbarrier that nothing completes for limit_ns, then
+// records a wait timeout (selftest.cu).
+cudaError_t fp8moe_launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);

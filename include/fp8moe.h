@@ -232,6 +232,14 @@ int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M,
                                    float* sx, uint8_t* qd, float* sd, int32_t dout_fmt,
                                    fp8moe_stream_t stream);
 
+/* Exercises the failure path of the bounded pipeline waits: one thread waits on
+ * an mbarrier that nothing ever completes, gives up after limit_us
+ * microseconds (1 .. 2,000,000, else FP8MOE_EINVAL), records
+ * FP8MOE_STATUS_WAIT_TIMEOUT with where = 6 (bits 8..15) in the status word and
+ * exits; the context stays usable.  For tests of failure detection; the paper
+ * has no counterpart. */
+int fp8moe_selftest_wait_timeout(uint32_t limit_us, fp8moe_stream_t stream);
+
 /* Waits for `stream`, returns in *flags the OR of the FP8MOE_STATUS_* bits set
  * since the last call, and clears them. */
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags);

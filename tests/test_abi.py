@@ -62,6 +62,15 @@ def test_argument_checks_run_before_any_device_call():
     assert L.fp8moe_gmm_dlhs_fp8_path(P(16), 64, 512, P(16), P(16), 4, 256, P(16), P(16), 1,
                                       None) == -1     # cached path needs N <= 256
     assert L.fp8moe_dequantize_fp8_codes(P(16), P(16), 4, 256, 8, P(16), None) == -2
+    # argument checks of the entry points added for the next steps of the path
+    assert L.fp8moe_selftest_wait_timeout(0, None) == -1              # limit must be > 0
+    assert L.fp8moe_selftest_wait_timeout(3000000, None) == -1        # and <= 2 s
+    assert L.fp8moe_gmm_fp8_fwd_block(P(16), 128, 512, P(16), P(16), 2, 256, P(16), P(16),
+                                      P(256), 10 ** 9, 256, 0, None) == -1   # block must be 512
+    assert L.fp8moe_tgmm_drhs_quant_fmt(P(16), P(16), 128, 64, 64, 1, P(16), P(16), P(256),
+                                        10 ** 9, 7, None) == -1       # unknown dout format
+    assert L.fp8moe_gmm_dlhs_dswiglu_fp8(P(16), 128, 256, P(16), P(16), 2, 64, None, P(16),
+                                         P(16), None, 0, None) == -1  # gu missing
 
 
 def test_build_is_up_to_date():

@@ -509,3 +509,22 @@ def test_tgmm_quantize_quotient_stress_bit_exact(orc):
     assert bad == 0
     assert torch.equal(sxt.cpu()[:nseg], rsx[:nseg]) and torch.equal(qx.cpu()[:nseg], rqx[:nseg])
     assert torch.equal(sd.cpu()[:nseg], rsd[:nseg]) and torch.equal(qd.cpu()[:nseg], rqd[:nseg])
+
+
+# ------------------------------------------------- failure detection (GPU)
+def test_bounded_wait_times_out_records_status_and_context_survives(orc):
+    """A wait that nothing completes gives up after its limit, records the
+    timeout (where = 6) in the status word, and the next call works: the
+    failure path of every pipeline wait, made to run out on purpose."""
+    import time
+    t0 = time.time()
+    fb.selftest_wait_timeout(20000)                  # 20 ms
+    st = fb.read_status()
+    assert time.time() - t0 < 5.0
+    assert st & fb.STATUS_WAIT_TIMEOUT
+    assert (st >> 8) & 0xFF == 6
+    assert fb.read_status() == 0                     # read clears
+    codes, scale = W.fp8_weights(2, 64, 32, 0.05, 9, device=DEV)
+    out = fb.dequantize_fp8_codes(codes, scale)
+    ref = orc.dequantize(codes.cpu(), scale.cpu())
+    assert torch.equal(bits16(out), bits16(ref))
