@@ -370,6 +370,15 @@ static int tgmm_drhs_impl(const void* lhs, const void* dout, int64_t M, int64_t 
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
+  {
+    // dW as [E][K][N] so that a box's rows past K (ragged k tile) are clipped
+    const uint64_t dims[3] = {(uint64_t)N, (uint64_t)K, (uint64_t)E};
+    const uint64_t st[2] = {(uint64_t)N * 4, (uint64_t)K * (uint64_t)N * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    rc = make_tmap(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dW, dims, st, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
   a.sx = w.sx;
   a.sd = w.sd;
   a.gs = group_sizes;

@@ -125,10 +125,6 @@ __device__ __forceinline__ Unit decode_unit(const Smem& s, int E, int nt, int u)
   return r;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // Dequantize a [256 x 64] codes tile (row r at r*64 bytes) into the K-major
 // 128-byte-swizzled bf16 operand (row r at r*128 bytes, 16-byte chunk c stored at
 // chunk c ^ (r & 7)). Thread t of the 256 dequant threads converts the 16-code

@@ -70,10 +70,6 @@ struct Smem {
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 struct Unit {
   int e, row0, rows, j;   // row0 / rows: this CTA's m tile (rows may be <= 0)
 };

@@ -55,6 +55,7 @@ cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int cached
 struct TgmmArgs {
   CUtensorMap tmX;        // qx slots [S, 128, K] u8
   CUtensorMap tmD;        // qd slots [S, 128, N] u8
+  CUtensorMap tmW;        // dW [E, K, N] f32 (store)
   const float* sx;        // [S, K]
   const float* sd;        // [S, N]
   const int32_t* gs;
