@@ -25,10 +25,11 @@
 //   warps 4..19 rescale: each thread owns one k row and 64 n columns of the f32
 //               accumulator in registers, acc += (sx * sd[n]) * P[n] in packed
 //               f32x2 instructions, reading the partial product from TMEM 16
-//               columns at a time. At the end of
-//               the unit each warp writes its [32 x 64] block to dW as two
-//               [32 x 32] TMA tensor stores from a swizzled shared-memory
-//               buffer, so the stores drain while the next unit computes.
+//               columns at a time. At the end of the unit each warp writes its
+//               [32 x 64] block to dW: the second 32 columns by coalesced
+//               stores through a swizzled shared-memory buffer, then the first
+//               32 columns by a TMA tensor store from the same buffer, which
+//               drains while the next unit computes.
 // The per-segment rescale costs as many FP32 lane operations as the FP8 MMA
 // takes tensor cycles, so the tile is as wide as the registers allow (64
 // accumulators a thread; warpgroup 0 of producer, MMA and two idle warps gives
@@ -140,6 +141,7 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
       if (e < E) s.segbase[e] = carry + incl - n;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
+    fence_proxy_async_smem();   // the staged group bounds precede TMA use of the buffers
     if (lane == 0) {
       s.segbase[E] = carry;
       s.total_units = E * units_per_e;
@@ -317,29 +319,44 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         ++used;
       }
       if (failed) break;
-      // store the [32 k rows x 64 n] block as two [32 x 32] boxes: each goes
-      // through the per-warp buffer in the 128-byte swizzled layout (16-byte
-      // chunk c4 of row i at chunk c4 ^ (i & 7)) and out by a TMA tensor store,
-      // which clips rows past K and columns past N
+      // store the [32 k rows x 64 n] block through the per-warp buffer, kept in
+      // the 128-byte swizzled layout (16-byte chunk c4 of row i at chunk
+      // c4 ^ (i & 7)): columns 32..63 first by coalesced 128-byte row stores,
+      // then columns 0..31 by a TMA tensor store (rows past K and columns past
+      // N clipped) that leaves the buffer while the next unit computes.
       const int k_warp0 = kt * kBK + quarter * 32;
+      const int n_w0 = ntile * kBN + cg * kCols;
+      if (lane == 0) bulk_wait_read();   // the previous unit's box has left the buffer
+      __syncwarp();
 #pragma unroll
-      for (int h = 0; h < kCols / 32; ++h) {
-        const int n_h0 = ntile * kBN + cg * kCols + h * 32;
-        if (lane == 0) bulk_wait_read();   // the previous box has left the buffer
-        __syncwarp();
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const int pc = c4 ^ (lane & 7);
+        *reinterpret_cast<float4*>(xp + lane * 32 + pc * 4) =
+            make_float4(a[32 + c4 * 4], a[32 + c4 * 4 + 1], a[32 + c4 * 4 + 2], a[32 + c4 * 4 + 3]);
+      }
+      __syncwarp();
+#pragma unroll 1
+      for (int it = 0; it < 8; ++it) {
+        const int i = it * 4 + (lane >> 3);       // row within the 32-row block
+        const int c4 = lane & 7;
+        const float4 v = *reinterpret_cast<const float4*>(xp + i * 32 + ((c4 ^ (i & 7)) * 4));
+        const int kk = k_warp0 + i;
+        const int nn = n_w0 + 32 + c4 * 4;
+        if (kk < K && nn < N)   // N % 16 == 0: a 4-column group is all in or all out
+          *reinterpret_cast<float4*>(dW + ((int64_t)e * K + kk) * N + nn) = v;
+      }
+      __syncwarp();
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const int pc = c4 ^ (lane & 7);
-          *reinterpret_cast<float4*>(xp + lane * 32 + pc * 4) =
-              make_float4(a[h * 32 + c4 * 4], a[h * 32 + c4 * 4 + 1], a[h * 32 + c4 * 4 + 2],
-                          a[h * 32 + c4 * 4 + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && k_warp0 < K && n_h0 < N) {
-          tma_store_3d(&tmW, xp, n_h0, k_warp0, e);
-          bulk_commit();
-        }
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const int pc = c4 ^ (lane & 7);
+        *reinterpret_cast<float4*>(xp + lane * 32 + pc * 4) =
+            make_float4(a[c4 * 4], a[c4 * 4 + 1], a[c4 * 4 + 2], a[c4 * 4 + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && k_warp0 < K && n_w0 < N) {
+        tma_store_3d(&tmW, xp, n_w0, k_warp0, e);
+        bulk_commit();
       }
     }
     if (lane == 0) bulk_wait();
