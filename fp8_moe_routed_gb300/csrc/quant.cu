@@ -290,23 +290,36 @@ __device__ __forceinline__ void build_segments_warp0(const int32_t* s_begin, con
 }
 
 // Work unit = (segment, 128-column chunk) over the columns of lhs then dout.
-// The segment's rows of the chunk are staged once in shared memory (one HBM
-// read), the per-column amax comes from there, then every thread casts its own
-// 16-byte pieces into the zero-padded slot.
+// The segment's rows of the chunk are staged once in shared memory by cp.async
+// (one HBM read, no staging registers), the per-column amax comes from there,
+// then every thread casts its own 16-byte pieces into the zero-padded slot.
+// Shared memory is the staged tile plus per-expert bounds sized by E, so that
+// several CTAs per SM keep loads in flight while others compute.
 constexpr int kTQThreads = 256;
+constexpr int kTQMinBlocks = 4;            // CTAs per SM the register budget allows
 constexpr int kTQCols = 128;
 constexpr int kTQRowBytes = kTQCols * 2;   // 256 B of bf16 per staged row
+constexpr size_t kTQTileBytes = 128 * (size_t)kTQRowBytes;      // 32 KB
+constexpr size_t kTQPartBytes = 4 * (kTQCols / 2) * 4;          // bf16x2 partial amax
+// dynamic shared memory: [tile][part][scale][begin E][end E][segbase E + 1]
+__host__ __device__ constexpr size_t tq_smem_bytes(int E) {
+  return kTQTileBytes + kTQPartBytes + kTQCols * 4 + (size_t)(3 * E + 1) * 4;
+}
 
-__global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
+__global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_kernel(
     const __nv_bfloat16* __restrict__ lhs, const __nv_bfloat16* __restrict__ dout, int64_t M,
     int K, int N, const int32_t* __restrict__ gs, int E, int64_t Smax,
     uint8_t* __restrict__ qx, float* __restrict__ sx, uint8_t* __restrict__ qd,
     float* __restrict__ sd, int report, int d_fmt) {
-  __shared__ int32_t s_begin[kMaxExperts], s_end[kMaxExperts], s_segbase[kMaxExperts + 1];
+  extern __shared__ __align__(16) uint8_t tq_smem[];
+  uint8_t* s_tile = tq_smem;                                     // [row][128 bf16]
+  uint32_t(*s_part)[kTQCols / 2] =
+      reinterpret_cast<uint32_t(*)[kTQCols / 2]>(tq_smem + kTQTileBytes);
+  float* s_scale = reinterpret_cast<float*>(tq_smem + kTQTileBytes + kTQPartBytes);
+  int32_t* s_begin = reinterpret_cast<int32_t*>(s_scale + kTQCols);
+  int32_t* s_end = s_begin + E;
+  int32_t* s_segbase = s_end + E;
   __shared__ int32_t s_T;
-  __shared__ __align__(16) uint8_t s_tile[128 * kTQRowBytes];   // [row][128 bf16]
-  __shared__ uint32_t s_part[4][kTQCols / 2];                   // bf16x2 partial amax
-  __shared__ float s_scale[kTQCols];
   load_groups_warp0(gs, E, M, s_begin, s_end, &s_T, report && blockIdx.x == 0);
   __syncthreads();
   build_segments_warp0(s_begin, s_end, E, s_segbase);
@@ -338,19 +351,14 @@ __global__ void __launch_bounds__(kTQThreads) tgmm_quantize_tiles_kernel(
     float* so = (is_x ? sx : sd) + (int64_t)qi * C;
     const bool pin = piece * 8 < ncols;
     // stage: rows [lo, hi) of the slot, 16 threads per 256-byte row
-    uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int rr = prow + 16 * i;
       if (pin && rr >= lo && rr < hi)
-        v[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(t * 128 + rr) * C + c0) + piece);
+        cp_async16(s_tile + rr * kTQRowBytes + piece * 16,
+                   src + (int64_t)(t * 128 + rr) * C + c0 + piece * 8, 16u);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = prow + 16 * i;
-      if (pin && rr >= lo && rr < hi)
-        *reinterpret_cast<uint4*>(s_tile + rr * kTQRowBytes + piece * 16) = v[i];
-    }
+    cp_async_wait_all();
     __syncthreads();
     // column amax: thread -> column pair cp, rows of quarter rq
     {
@@ -460,8 +468,14 @@ cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
                                               int num_sms, int report, int d_fmt, cudaStream_t s) {
   using namespace fp8moe;
-  int grid = num_sms * 6;
-  tgmm_quantize_tiles_kernel<<<grid, kTQThreads, 0, s>>>(
+  const size_t smem = tq_smem_bytes(E);   // < 48 KB for any E <= kMaxExperts
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, tgmm_quantize_tiles_kernel, kTQThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const int grid = num_sms * per_sm;   // one resident wave, grid-stride over units
+  tgmm_quantize_tiles_kernel<<<grid, kTQThreads, smem, s>>>(
       static_cast<const __nv_bfloat16*>(lhs), static_cast<const __nv_bfloat16*>(dout), M, K, N,
       gs, E, Smax, qx, sx, qd, sd, report, d_fmt);
   return cudaGetLastError();
