@@ -300,10 +300,14 @@ constexpr int kTQMinBlocks = 4;            // CTAs per SM the register budget al
 constexpr int kTQCols = 128;
 constexpr int kTQRowBytes = kTQCols * 2;   // 256 B of bf16 per staged row
 constexpr size_t kTQTileBytes = 128 * (size_t)kTQRowBytes;      // 32 KB
-constexpr size_t kTQPartBytes = 4 * (kTQCols / 2) * 4;          // bf16x2 partial amax
-// dynamic shared memory: [tile][part][scale][begin E][end E][segbase E + 1]
+constexpr int kTQPieces = kTQCols / 8;                         // 16-byte pieces per staged row
+constexpr int kTQRowStep = kTQThreads / kTQPieces;              // rows between a thread's rows
+constexpr int kTQRowsPer = 128 / kTQRowStep;                    // rows per thread
+constexpr size_t kTQPartBytes = (kTQThreads / 32) * kTQPieces * 16;   // per warp and piece: 4 bf16x2 amax
+static_assert(kTQPieces <= 32 && kTQRowsPer * kTQRowStep == 128, "tile geometry");
+// dynamic shared memory: [tile][part][scale][rl][rh][begin E][end E][segbase E + 1]
 __host__ __device__ constexpr size_t tq_smem_bytes(int E) {
-  return kTQTileBytes + kTQPartBytes + kTQCols * 4 + (size_t)(3 * E + 1) * 4;
+  return kTQTileBytes + kTQPartBytes + 3 * kTQCols * 4 + (size_t)(3 * E + 1) * 4;
 }
 
 __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_kernel(
@@ -313,10 +317,11 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
     float* __restrict__ sd, int report, int d_fmt) {
   extern __shared__ __align__(16) uint8_t tq_smem[];
   uint8_t* s_tile = tq_smem;                                     // [row][128 bf16]
-  uint32_t(*s_part)[kTQCols / 2] =
-      reinterpret_cast<uint32_t(*)[kTQCols / 2]>(tq_smem + kTQTileBytes);
+  uint4* s_part = reinterpret_cast<uint4*>(tq_smem + kTQTileBytes);   // [warp][piece]
   float* s_scale = reinterpret_cast<float*>(tq_smem + kTQTileBytes + kTQPartBytes);
-  int32_t* s_begin = reinterpret_cast<int32_t*>(s_scale + kTQCols);
+  float* s_rl = s_scale + kTQCols;                               // quotient brackets per column
+  float* s_rh = s_rl + kTQCols;
+  int32_t* s_begin = reinterpret_cast<int32_t*>(s_rh + kTQCols);
   int32_t* s_end = s_begin + E;
   int32_t* s_segbase = s_end + E;
   __shared__ int32_t s_T;
@@ -332,10 +337,13 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
   const int ck = (K + kTQCols - 1) / kTQCols, cn = (N + kTQCols - 1) / kTQCols, cpq = ck + cn;
   const int64_t units = (int64_t)S * cpq;
   const int tid = threadIdx.x;
-  const int piece = tid & 15;         // 16-byte piece (8 columns) of a staged row
-  const int prow = tid >> 4;          // first row of this thread, step 16
+  const int piece = tid % kTQPieces;  // 16-byte piece (8 columns) of a staged row
+  const int prow = tid / kTQPieces;   // first row of this thread, step kTQRowStep
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool small = units < (int64_t(1) << 31);   // 32-bit unit arithmetic
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int qi = (int)(u / cpq), ch = (int)(u % cpq);
+    const int qi = small ? (int)((uint32_t)u / (uint32_t)cpq) : (int)(u / cpq);
+    const int ch = (int)(u - (int64_t)qi * cpq);
     const int e = find_bucket(s_segbase, E, qi);
     const int t = s_begin[e] / 128 + (qi - s_segbase[e]);
     const int r0 = max(s_begin[e], t * 128), r1 = min(s_end[e], t * 128 + 128);
@@ -347,37 +355,60 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
     const int c0 = (is_x ? ch : ch - ck) * kTQCols;
     const int ncols = min(kTQCols, C - c0);                     // multiple of 16
     const __nv_bfloat16* src = is_x ? lhs : dout;
-    uint8_t* qo = (is_x ? qx : qd) + (int64_t)qi * 128 * C;
+    uint8_t* qo = (is_x ? qx : qd) + (int64_t)qi * 128 * C + c0 + piece * 8;
     float* so = (is_x ? sx : sd) + (int64_t)qi * C;
     const bool pin = piece * 8 < ncols;
     // stage: rows [lo, hi) of the slot, 16 threads per 256-byte row
+    if (pin) {
+      const __nv_bfloat16* sp = src + (int64_t)(t * 128 + prow) * C + c0 + piece * 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = prow + 16 * i;
-      if (pin && rr >= lo && rr < hi)
-        cp_async16(s_tile + rr * kTQRowBytes + piece * 16,
-                   src + (int64_t)(t * 128 + rr) * C + c0 + piece * 8, 16u);
+      for (int i = 0; i < kTQRowsPer; ++i) {
+        const int rr = prow + kTQRowStep * i;
+        if (rr >= lo && rr < hi)
+          cp_async16(s_tile + rr * kTQRowBytes + piece * 16, sp + (int64_t)kTQRowStep * i * C, 16u);
+      }
     }
     cp_async_wait_all();
     __syncthreads();
-    // column amax: thread -> column pair cp, rows of quarter rq
+    // column amax over the segment rows (exact): each thread reduces the rows
+    // of its 16-byte piece that it casts later, the row sets of a warp meet by
+    // shuffle and the warps' partials in shared memory
     {
-      const int cp = tid & 63, rq = tid >> 6;
-      uint32_t m2 = 0;
-      const int a = max(lo, rq * 32), b = min(hi, rq * 32 + 32);
-      for (int rr = a; rr < b; ++rr)
-        m2 = bf16x2_absmax(m2, *reinterpret_cast<const uint32_t*>(s_tile + rr * kTQRowBytes + cp * 4));
-      s_part[rq][cp] = m2;
+      uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+      if (pin) {
+#pragma unroll
+        for (int i = 0; i < kTQRowsPer; ++i) {
+          const int rr = prow + kTQRowStep * i;
+          if (rr >= lo && rr < hi) {
+            const uint4 x = *reinterpret_cast<const uint4*>(s_tile + rr * kTQRowBytes + piece * 16);
+            m0 = bf16x2_absmax(m0, x.x);
+            m1 = bf16x2_absmax(m1, x.y);
+            m2 = bf16x2_absmax(m2, x.z);
+            m3 = bf16x2_absmax(m3, x.w);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = kTQPieces; o < 32; o <<= 1) {
+        m0 = bf16x2_absmax(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = bf16x2_absmax(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        m2 = bf16x2_absmax(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+        m3 = bf16x2_absmax(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+      }
+      if (lane < kTQPieces) s_part[warp * kTQPieces + lane] = make_uint4(m0, m1, m2, m3);
     }
     __syncthreads();
-    if (tid < kTQCols / 2) {
-      uint32_t m2 = s_part[0][tid];
+    if (tid < kTQCols / 2) {   // column pair tid = word tid % 4 of piece tid / 4
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(s_part) + (tid >> 2) * 4 + (tid & 3);
+      uint32_t m2 = 0;
 #pragma unroll
-      for (int i = 1; i < 4; ++i) m2 = bf16x2_absmax(m2, s_part[i][tid]);
+      for (int w = 0; w < kTQThreads / 32; ++w) m2 = bf16x2_absmax(m2, pw[w * kTQPieces * 4]);
       const float s0 = __fdiv_rn(fmaxf(bf16lo_to_f32(m2), kEps), fmax);
       const float s1 = __fdiv_rn(fmaxf(bf16hi_to_f32(m2), kEps), fmax);
       s_scale[2 * tid] = s0;
       s_scale[2 * tid + 1] = s1;
+      bracket(s0, s_rl[2 * tid], s_rh[2 * tid]);
+      bracket(s1, s_rl[2 * tid + 1], s_rh[2 * tid + 1]);
       if (2 * tid < ncols) {
         so[c0 + 2 * tid] = s0;
         so[c0 + 2 * tid + 1] = s1;
@@ -388,13 +419,17 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
     if (pin) {
       float sc[8], rl[8], rh[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc[j] = s_scale[piece * 8 + j];
-        bracket(sc[j], rl[j], rh[j]);
+      for (int j = 0; j < 8; j += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(s_scale + piece * 8 + j);
+        const float4 b = *reinterpret_cast<const float4*>(s_rl + piece * 8 + j);
+        const float4 c = *reinterpret_cast<const float4*>(s_rh + piece * 8 + j);
+        sc[j] = a.x; sc[j + 1] = a.y; sc[j + 2] = a.z; sc[j + 3] = a.w;
+        rl[j] = b.x; rl[j + 1] = b.y; rl[j + 2] = b.z; rl[j + 3] = b.w;
+        rh[j] = c.x; rh[j + 1] = c.y; rh[j + 2] = c.z; rh[j + 3] = c.w;
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = prow + 16 * i;
+      for (int i = 0; i < kTQRowsPer; ++i) {
+        const int rr = prow + kTQRowStep * i;
         uint2 o = make_uint2(0u, 0u);
         if (rr >= lo && rr < hi) {
           const uint4 x = *reinterpret_cast<const uint4*>(s_tile + rr * kTQRowBytes + piece * 16);
@@ -416,7 +451,7 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
           o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
           o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
         }
-        *reinterpret_cast<uint2*>(qo + (int64_t)rr * C + c0 + piece * 8) = o;
+        *reinterpret_cast<uint2*>(qo + (int64_t)rr * C) = o;
       }
     }
     __syncthreads();   // the tile and scales are reused by the next unit
