@@ -493,7 +493,7 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (CACHED) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&s.tempty[acc]);
+          if (lane == 0) mbar_arrive_relaxed(&s.tempty[acc]);
           acc ^= 1;
           if (acc == 0) aph ^= 1;
         }
@@ -501,7 +501,7 @@ gmm_dlhs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!CACHED && ok) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s.tempty[0]);
+        if (lane == 0) mbar_arrive_relaxed(&s.tempty[0]);
         aph ^= 1;
       }
     }

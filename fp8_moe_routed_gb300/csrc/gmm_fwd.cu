@@ -345,7 +345,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[acc]), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&s.tempty[acc]), 0));
           }
           acc ^= 1;
           if (acc == 0) aph ^= 1;
@@ -459,7 +459,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       // the even CTA's MMA thread waits for the epilogue warps of both CTAs
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.tempty[acc]), 0));
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&s.tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) aph ^= 1;
       sb ^= 1;

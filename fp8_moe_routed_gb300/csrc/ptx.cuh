@@ -39,6 +39,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive without release semantics, for a barrier that only reports "this warp
+// has finished reading a TMEM buffer": after tcgen05.wait::ld the loads are
+// complete and the values are in registers, so no write of this thread has to
+// become visible to the waiter (the MMA that overwrites the buffer), while a
+// release would first wait for this thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
@@ -353,6 +362,13 @@ __device__ __forceinline__ void cluster_sync() {
 // Arrive on an mbarrier given by its shared::cluster address (possibly the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               ::"r"(cluster_addr) : "memory");
+}
+// The relaxed form of mbar_arrive_cluster (see mbar_arrive_relaxed): a release at
+// cluster scope waits until this thread's earlier global stores are visible to
+// the whole cluster, which after an epilogue's tile of stores is microseconds.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
                ::"r"(cluster_addr) : "memory");
 }
 

@@ -304,7 +304,7 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
           if (c == kCols / kChunk - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s.tempty[acc]);   // TMEM buffer free once in registers
+            if (lane == 0) mbar_arrive_relaxed(&s.tempty[acc]);   // TMEM buffer free once in registers
           }
 #pragma unroll
           for (int i = 0; i < kChunk / 4; ++i) {
