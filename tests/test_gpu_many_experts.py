@@ -1,0 +1,116 @@
+"""GPU parity at a large expert count: 1000 experts, nearly all empty, the
+non-empty ones spread past the 32-expert chunks of the group scans (indices 3,
+40, 64, 511, 998, 999), one with a single row and one straddling several
+128-row tiles, plus tail garbage past T. Every entry point is checked against
+the oracle: row quantization and the tgmm tile quantization bit-exact, the
+GMMs within the stated tolerances, and rows past T (and experts without rows)
+untouched or zero as documented."""
+import pytest
+import torch
+
+from fp8_moe_routed_gb300 import binding as fb
+from fp8_moe_routed_gb300 import workloads as W
+from parity_util import bits16, check_bf16, check_f32_rel
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+E = 1000
+M = 800
+SIZES = {3: 130, 40: 1, 64: 257, 511: 100, 998: 200, 999: 45}   # T = 733
+
+
+def group_sizes():
+    gs = torch.zeros(E, dtype=torch.int32)
+    for e, n in SIZES.items():
+        gs[e] = n
+    return gs
+
+
+def cuda(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fb.load()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    fb.read_status()
+    yield
+    assert fb.read_status() == 0
+
+
+def test_many_experts_quantize_rows_bit_exact(orc):
+    K = 512
+    gs = group_sizes()
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=71, outlier_frac=0.02), T)
+    q, sx = fb.quantize_rows(*cuda(x, gs))
+    q_ref, sx_ref, bad = orc.quantize_rows(x, gs)
+    assert bad == 0
+    assert torch.equal(q.cpu()[:T], q_ref[:T])
+    assert torch.equal(sx.cpu()[:T], sx_ref[:T])
+
+
+@pytest.mark.parametrize("silu", [True, False])
+def test_many_experts_gmm_fwd(orc, silu):
+    K, N = 256, 256
+    gs = group_sizes()
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=72, outlier_frac=0.01), T)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=73)
+    Nout = N // 2 if silu else N
+    out = torch.full((M, Nout), 7.0, dtype=torch.bfloat16, device=DEV)
+    fn = fb.gmm_silu_fp8_fwd if silu else fb.gmm_fp8_fwd
+    fn(*cuda(x, codes, scale, gs), out=out)
+    ref, _, bad = orc.gmm_fwd(x, codes, scale, gs, silu=silu)
+    assert bad == 0
+    check_bf16(out[:T], ref[:T], what=f"fwd E=1000 silu={silu}")
+    assert (out[T:].float() == 7.0).all(), "rows >= T were written"
+
+
+def test_many_experts_dlhs_both_paths(orc):
+    N, K = 256, 384
+    gs = group_sizes()
+    T = int(gs.sum())
+    dout = W.fill_tail_garbage(W.cotangent(M, N, seed=74), T)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=75)
+    args = cuda(dout, codes, scale, gs)
+    out0 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out0, path=0)
+    ref, _, bad = orc.gmm_dlhs(dout, codes, scale, gs)
+    assert bad == 0
+    check_bf16(out0[:T], ref[:T], what="dlhs E=1000")
+    assert (out0[T:].float() == 7.0).all()
+    out1 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out1, path=1)
+    assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
+
+
+def test_many_experts_tgmm(orc):
+    K, N = 128, 144
+    gs = group_sizes()
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=76), T)
+    d = W.fill_tail_garbage(W.cotangent(M, N, seed=77), T)
+    xg, dg, gsg = cuda(x, d, gs)
+    qx, sx, qd, sd = fb.tgmm_quantize_tiles(xg, dg, gsg)
+    qx_r, sx_r, qd_r, sd_r, nseg, bad = orc.tgmm_quantize_tiles(x, d, gs)
+    assert bad == 0
+    assert torch.equal(qx.cpu()[:nseg], qx_r[:nseg]) and torch.equal(qd.cpu()[:nseg], qd_r[:nseg])
+    assert torch.equal(sx.cpu()[:nseg], sx_r[:nseg]) and torch.equal(sd.cpu()[:nseg], sd_r[:nseg])
+    dw = fb.tgmm_drhs_quant(xg, dg, gsg)
+    ref, bad = orc.tgmm(x, d, gs)
+    assert bad == 0
+    assert torch.isfinite(dw).all()
+    check_f32_rel(dw, ref, what="tgmm E=1000")
+    empty = torch.ones(E, dtype=torch.bool)
+    empty[list(SIZES)] = False
+    assert (dw[empty.to(DEV)] == 0).all(), "experts without rows must get dW = 0"
