@@ -98,6 +98,53 @@ __device__ __forceinline__ uint2 quant8(uint4 v, float s, float rl, float rh) {
 // many rows in flight per SM, which is what an HBM-bound pass needs.
 constexpr int kQThreads = 256;
 
+// Rows of at most 2048 columns: a warp per row, the row in the registers of its
+// 32 lanes, so the amax needs only shuffles (no block barrier) and dozens of rows
+// per SM are in flight. Same arithmetic as quantize_rows_kernel.
+template <int CPL>
+__global__ void __launch_bounds__(kQThreads) quantize_rows_warp_kernel(
+    const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
+    int E, int e0, int e1, uint8_t* __restrict__ q, float* __restrict__ sx, int report) {
+  __shared__ int32_t s_lo, s_hi;
+  group_row_range_warp0(gs, E, M, e0, e1, &s_lo, &s_hi, report && blockIdx.x == 0);
+  __syncthreads();
+  const int64_t lo = s_lo, T = s_hi;   // rows [lo, T) of experts [e0, e1)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = K >> 3;           // K % 8 == 0
+  constexpr int kWarps = kQThreads / 32;
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  for (int64_t m = lo + (int64_t)blockIdx.x * kWarps + warp; m < T; m += stride) {
+    const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
+    uint4 v[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      v[i] = c < nchunk ? __ldg(row + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t amax2 = 0;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      amax2 = bf16x2_absmax(amax2, v[i].x);
+      amax2 = bf16x2_absmax(amax2, v[i].y);
+      amax2 = bf16x2_absmax(amax2, v[i].z);
+      amax2 = bf16x2_absmax(amax2, v[i].w);
+    }
+    float amax = bf16x2_hmax_to_f32(amax2);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float s = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
+    float rl, rh;
+    bracket(s, rl, rh);
+    uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nchunk) qrow[c] = quant8(v[i], s, rl, rh);
+    }
+    if (lane == 0) sx[m] = s;
+  }
+}
+
 template <int CPT>
 __global__ void __launch_bounds__(kQThreads) quantize_rows_kernel(
     const __nv_bfloat16* __restrict__ lhs, int64_t M, int K, const int32_t* __restrict__ gs,
@@ -472,6 +519,26 @@ cudaError_t fp8moe_launch_quantize_rows(const void* lhs, int64_t M, int K, const
   int grid = (int)(M < cap ? M : cap);
   if (grid < 1) grid = 1;
   const auto* x = static_cast<const __nv_bfloat16*>(lhs);
+  const int cpl = (K / 8 + 31) / 32;   // 16-byte chunks per lane of a warp-per-row kernel
+  if (cpl <= 8) {
+    // a warp per row; one resident wave of CTAs (at most ctas_per_sm per SM)
+    // strides over the rows by warps
+    auto run = [&](auto kern) -> cudaError_t {
+      int per_sm = 0;
+      cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, 0);
+      if (err != cudaSuccess) return err;
+      per_sm = per_sm < 1 ? 1 : (per_sm > ctas_per_sm ? ctas_per_sm : per_sm);
+      const int64_t need = (M + kQThreads / 32 - 1) / (kQThreads / 32);
+      const int64_t wave = (int64_t)num_sms * per_sm;
+      const int g = (int)(need < wave ? (need < 1 ? 1 : need) : wave);
+      kern<<<g, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
+      return cudaGetLastError();
+    };
+    if (cpl <= 1) return run(quantize_rows_warp_kernel<1>);
+    if (cpl <= 2) return run(quantize_rows_warp_kernel<2>);
+    if (cpl <= 4) return run(quantize_rows_warp_kernel<4>);
+    return run(quantize_rows_warp_kernel<8>);
+  }
   const int cpt = (K / 8 + kQThreads - 1) / kQThreads;
   if (cpt <= 1)
     quantize_rows_kernel<1><<<grid, kQThreads, 0, s>>>(x, M, K, gs, E, e0, e1, q, sx, report);
