@@ -184,9 +184,7 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int r, bool row_ok,
     const int col0 = col_base + c * 32;
     if (row_ok) {
       if (col0 + 32 <= K) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        st_global_64B(orow + col0, o);
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
 #pragma unroll

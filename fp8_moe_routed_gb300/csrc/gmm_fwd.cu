@@ -103,9 +103,7 @@ __device__ __forceinline__ void store_row_chunk(const uint32_t* o, bool row_ok,
                                                 int Nout) {
   if (!row_ok) return;
   if (col0 + 32 <= Nout) {
-    uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    st_global_64B(orow + col0, o);
   } else {
     uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
 #pragma unroll
@@ -442,18 +440,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             col0 = t.j * kBN + c * 32;
           }
-          if (row_ok) {
-            if (col0 + 32 <= Nout) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            } else {
-              uint16_t* dst = reinterpret_cast<uint16_t*>(orow);
-#pragma unroll
-              for (int q = 0; q < 32; ++q)
-                if (col0 + q < Nout) dst[col0 + q] = (uint16_t)(o[q / 2] >> (16 * (q & 1)));
-            }
-          }
+          store_row_chunk(o, row_ok, orow, col0, Nout);
         }
       }
       tc_fence_before();

@@ -157,6 +157,26 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// 64 bytes (16 words, e.g. 32 bf16) to global memory: two 32-byte stores when p
+// is 32-byte aligned, else four 16-byte stores. Epilogues where each thread
+// writes its own row touch one row per lane, so the wider stores halve the
+// memory transactions of a warp.
+__device__ __forceinline__ void st_global_64B(void* p, const uint32_t* o) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                   ::"l"(static_cast<char*>(p) + 32 * h), "r"(o[8 * h]), "r"(o[8 * h + 1]),
+                     "r"(o[8 * h + 2]), "r"(o[8 * h + 3]), "r"(o[8 * h + 4]), "r"(o[8 * h + 5]),
+                     "r"(o[8 * h + 6]), "r"(o[8 * h + 7])
+                   : "memory");
+  } else {
+    uint4* d = static_cast<uint4*>(p);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (the
 // tensor core reads its operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
