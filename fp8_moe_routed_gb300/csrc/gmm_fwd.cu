@@ -22,9 +22,12 @@
 //               completion is counted on the even CTA's barrier.
 //   warp 1      TMEM allocation for the pair (512 columns = two 128 x 256 f32
 //               accumulators per CTA); in the even CTA, the MMA-issuing thread.
-//   warps 2..5  epilogue of this CTA's 128 rows: tcgen05.ld, scales, SwiGLU,
-//               bf16, row-masked 16-byte stores; the second accumulator lets
-//               the next tile's MMAs run meanwhile.
+//   warps 2..    epilogue of this CTA's 128 rows: tcgen05.ld, scales, SwiGLU,
+//               bf16, row-masked 32-byte stores; the second accumulator lets
+//               the next tile's MMAs run meanwhile. Four warps (one per TMEM
+//               lane quarter) for the plain forward; eight (two per quarter,
+//               half the columns each) for SwiGLU and the block mode, whose
+//               heavier epilogues would otherwise hold up the MMAs.
 // SwiGLU: the even CTA's B half is the gate columns, the odd CTA's the matching
 // up columns, so accumulator columns [0, 128) are gate and [128, 256) up.
 // Units are enumerated expert by expert, n tile by n tile, pairs fastest, so
@@ -49,7 +52,19 @@ constexpr int kBN = 256;                    // accumulator columns (MMA N)
 constexpr int kABytes = kBM * 128;          // 16 KB: 128 rows x 128 bytes of K
 constexpr int kBBytes = 128 * 128;          // 16 KB: this CTA's 128 columns x 128 bytes of K
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
+// Epilogue warps: one per TMEM lane quarter (4), or two per quarter with half the
+// columns each (8) where the epilogue is heavy enough to hold up the MMAs
+// otherwise (SwiGLU; the block mode's per-block folding). Registers are budgeted
+// per SM sub-partition: 10 warps put 3 on two of them, so a thread may hold
+// 16384 / (3 * 32) -> 168 registers (launch bounds of 384 threads give the
+// compiler that cap); 6 warps put at most 2 on one, which leaves the cap at 255.
+template <bool SWIGLU, bool BLK>
+struct Epi {
+  static constexpr int kWarps = (SWIGLU || BLK) ? 8 : 4;
+  static constexpr int kHalves = kWarps / 4;
+  static constexpr int kThreads = (2 + kWarps) * 32;
+  static constexpr int kRegBudgetThreads = kWarps == 8 ? 384 : 192;
+};
 constexpr int kTmemCols = 512;
 
 struct Smem {
@@ -115,7 +130,7 @@ __device__ __forceinline__ void store_row_chunk(const uint32_t* o, bool row_ok,
 // FP8: a 128-byte swizzle row holds 128 K values of A (or 128 N values of B);
 // BF16: 64.
 template <bool FP8, bool SWIGLU, bool BLK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Epi<SWIGLU, BLK>::kRegBudgetThreads, 1)
 gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const float* __restrict__ sx, const float* __restrict__ scale,
                const int32_t* __restrict__ gs, __nv_bfloat16* __restrict__ out, int64_t M, int K,
@@ -165,7 +180,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 8);   // one elected lane per epilogue warp, both CTAs
+        mbar_init(&s.tempty[i], 2 * Epi<SWIGLU, BLK>::kWarps);   // one lane per epilogue warp, both CTAs
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -282,8 +297,11 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) mbar_wait_cluster(&s.drain, 0, kWhereDrain);
   } else {
     // =============================== epilogue =============================
-    const int et = threadIdx.x - 64;                 // 0..127
+    const int et = threadIdx.x - 64;                 // epilogue thread
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter ..
+    constexpr int kEpiThreads = Epi<SWIGLU, BLK>::kWarps * 32;
+    constexpr int kHalves = Epi<SWIGLU, BLK>::kHalves;
+    const int half = (warp - 2) >> 2;                // which half of the columns (8 warps)
     const int r = quarter * 32 + lane;               // row inside this CTA's tile
     int acc = 0;
     uint32_t aph = 0;
@@ -296,8 +314,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // per-column scales of this tile's 256 accumulator columns
       if (FP8) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = et + 128 * h;
+        for (int c = et; c < kBN; c += kEpiThreads) {
           int col;
           bool in;
           if (SWIGLU) {
@@ -310,14 +327,17 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           s.sw[sb][c] = in ? __ldg(scale + (int64_t)t.e * N + col) : 0.0f;
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpiThreads);
       const bool row_ok = r < t.rows;
       const int64_t row = (int64_t)t.row0 + r;
       if (BLK) {
         // ---- block mode: fold every block's accumulator into bf16 registers
-        uint32_t accb[kBN / 2];           // bf16 pairs of columns (2i, 2i + 1)
+        // bf16 pairs of this thread's 128 columns: SwiGLU gate chunks 2 half,
+        // 2 half + 1 in accb[0..31] and the matching up chunks in accb[32..63];
+        // otherwise chunks 4 half .. 4 half + 3
+        uint32_t accb[kBN / 4];
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) accb[i] = 0u;
+        for (int i = 0; i < kBN / 4; ++i) accb[i] = 0u;
         const int nblk = (nkb + kBlkSteps - 1) / kBlkSteps;
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
         for (int b = 0; b < nblk; ++b) {
@@ -328,9 +348,10 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (t.rows > 0) {
               const uint32_t tbase = trow + (uint32_t)(acc * kBN);
 #pragma unroll
-              for (int c = 0; c < kBN / 32; ++c) {
+              for (int c = 0; c < kBN / 64; ++c) {
+                const int tc = SWIGLU ? (c < 2 ? 2 * half + c : 4 + 2 * half + (c - 2)) : 4 * half + c;
                 uint32_t v[32];
-                tmem_ld32(tbase + c * 32, v);
+                tmem_ld32(tbase + tc * 32, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -352,34 +373,36 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           __nv_bfloat16* orow = out + row * Nout;
           if (SWIGLU) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
+              const int oc = 2 * half + c;        // output chunk of 32 columns
               uint32_t o[16];
 #pragma unroll
               for (int i = 0; i < 32; i += 2) {
                 float y[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                  const uint32_t gw = accb[(c * 32 + i) / 2], uw = accb[(128 + c * 32 + i) / 2];
+                  const uint32_t gw = accb[(c * 32 + i) / 2], uw = accb[32 + (c * 32 + i) / 2];
                   const float gg = __fmul_rn(h ? bf16hi_to_f32(gw) : bf16lo_to_f32(gw),
-                                             s.sw[sb][c * 32 + i + h]);
+                                             s.sw[sb][oc * 32 + i + h]);
                   const float uu = __fmul_rn(h ? bf16hi_to_f32(uw) : bf16lo_to_f32(uw),
-                                             s.sw[sb][128 + c * 32 + i + h]);
+                                             s.sw[sb][128 + oc * 32 + i + h]);
                   y[h] = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg))), uu);
                 }
                 o[i / 2] = f32x2_to_bf16x2(y[0], y[1]);
               }
-              store_row_chunk(o, row_ok, orow, t.j * 128 + c * 32, Nout);
+              store_row_chunk(o, row_ok, orow, t.j * 128 + oc * 32, Nout);
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < kBN / 64; ++c) {
+              const int oc = 4 * half + c;
               uint32_t o[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                o[i] = f32x2_to_bf16x2(__fmul_rn(bf16lo_to_f32(accb[c * 16 + i]), s.sw[sb][c * 32 + 2 * i]),
+                o[i] = f32x2_to_bf16x2(__fmul_rn(bf16lo_to_f32(accb[c * 16 + i]), s.sw[sb][oc * 32 + 2 * i]),
                                        __fmul_rn(bf16hi_to_f32(accb[c * 16 + i]),
-                                                 s.sw[sb][c * 32 + 2 * i + 1]));
-              store_row_chunk(o, row_ok, orow, t.j * kBN + c * 32, Nout);
+                                                 s.sw[sb][oc * 32 + 2 * i + 1]));
+              store_row_chunk(o, row_ok, orow, t.j * kBN + oc * 32, Nout);
             }
           }
         }
@@ -398,9 +421,10 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (t.rows > 0) {
         const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
         __nv_bfloat16* orow = out + row * Nout;
-        constexpr int kChunks = SWIGLU ? 4 : 8;
+        constexpr int kChunks = (SWIGLU ? 4 : 8) / kHalves;   // this warp's columns
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int c = half * kChunks + cc;
           uint32_t o[16];
           int col0;
           if (SWIGLU) {
@@ -469,7 +493,7 @@ cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);   // whole CTA pairs, one CTA per SM
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Epi<SWIGLU, BLK>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
