@@ -41,11 +41,11 @@ M = TOKENS * TOPK
 ROWS_PER_EXPERT = M // E
 METRIC = "FP8 GMM TFLOP/s (wi+SwiGLU fwd, wo fwd, dLHS) and % of GB300 FP8 peak"
 # DRAM bytes (read + write) of one wi forward call at 32 experts x 1024 rows,
-# K = 7168, N = 4096: quantize_rows_kernel<4> 469.8 + 202.9 MB and
-# gmm_fwd_kernel<1, 1> 1194.6 + 124.0 MB, from a one-pass ncu capture
+# K = 7168, N = 4096: quantize_rows_kernel<4> 469.8 + 202.7 MB and
+# gmm_fwd_kernel<1, 1, 0> 1290.9 + 124.8 MB, from a one-pass ncu capture
 # (dram__bytes_read.sum, dram__bytes_write.sum) of this bench's workload.
 # Valid for those two kernels as captured; set to None when either changes.
-WI_FWD_TRAFFIC = 2003.7e6
+WI_FWD_TRAFFIC = 2088.2e6
 WI_FWD_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi forward "
                          "(row quantizer + GMM), profiles/gmm_fwd_wi_e4_m4096_k7168_n4096.md")
 
