@@ -251,7 +251,7 @@ def gmm_silu_fp8_fwd_noalloc(lhs, codes, scale, group_sizes, out):
 
 def gmm_dlhs_fp8(dout, codes, scale, group_sizes, out=None, path: Optional[int] = None):
     """dLHS: bf16 [M, K] (see fp8moe_gmm_dlhs_fp8; path forces 0 streaming /
-    1 cached)."""
+    1 cached / 2 CTA pairs with the weight in tensor memory)."""
     L = load()
     _req(dout, torch.bfloat16, "dout", 2)
     _req(codes, torch.uint8, "codes", 3)
@@ -280,7 +280,7 @@ def gmm_dlhs_dswiglu_fp8(dout, codes, scale, gu, group_sizes, out=None,
                          path: Optional[int] = None):
     """wo dLHS + SwiGLU backward: dgu bf16 [M, 2F] from dout [M, N], the wo
     codes [E, F, N] and the wi output gu [M, 2F] (see fp8moe_gmm_dlhs_dswiglu_fp8;
-    path forces 0 streaming / 1 cached)."""
+    path forces 0 streaming / 1 cached / 2 CTA pairs)."""
     L = load()
     _req(dout, torch.bfloat16, "dout", 2)
     _req(codes, torch.uint8, "codes", 3)

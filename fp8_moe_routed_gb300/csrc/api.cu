@@ -232,6 +232,11 @@ int dlhs_impl(const void* dout, int64_t M, int64_t N, const uint8_t* codes, cons
     rc = make_tmap(&a.tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, codes, dims, st, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
+    // pair path: 128 k rows x 64 bytes, 64-byte swizzle (conflict-free row reads)
+    const uint32_t box_p[3] = {64, 128, 1};
+    rc = make_tmap(&a.tmCp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, codes, dims, st, box_p,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc) return rc;
   }
   a.scale = scale;
   a.gs = gs;
@@ -240,7 +245,7 @@ int dlhs_impl(const void* dout, int64_t M, int64_t N, const uint8_t* codes, cons
   a.N = (int)N;
   a.K = (int)K;
   a.E = E;
-  cudaError_t e = fp8moe_launch_gmm_dlhs(a, sms, path == 1, stream);
+  cudaError_t e = fp8moe_launch_gmm_dlhs(a, sms, path, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
 }
@@ -296,8 +301,9 @@ int fp8moe_gmm_dlhs_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* c
                         fp8moe_stream_t stream) {
   (void)workspace;
   (void)workspace_bytes;
-  // the on-chip cache path when the whole contraction fits one cached block
-  const int path = (N <= 256) ? 1 : 0;
+  // the on-chip cache path when the whole contraction fits one cached block,
+  // otherwise CTA pairs with the dequantized weight in tensor memory
+  const int path = (N <= 256) ? 1 : 2;
   return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, nullptr, dlhs, path, stream);
 }
 
@@ -305,7 +311,7 @@ int fp8moe_gmm_dlhs_fp8_path(const void* dout, int64_t M, int64_t N, const uint8
                              const float* scale, int32_t E, int64_t K,
                              const int32_t* group_sizes, void* dlhs, int32_t path,
                              fp8moe_stream_t stream) {
-  if (path != 0 && path != 1) return FP8MOE_EINVAL;
+  if (path < 0 || path > 2) return FP8MOE_EINVAL;
   return dlhs_impl(dout, M, N, codes, scale, E, K, group_sizes, nullptr, dlhs, path, stream);
 }
 
@@ -316,6 +322,8 @@ int fp8moe_gmm_dlhs_dswiglu_fp8(const void* dout, int64_t M, int64_t N, const ui
   (void)workspace;
   (void)workspace_bytes;
   if (M > 0 && !gu) return FP8MOE_EINVAL;
+  // the pair path's epilogue holds f32 values for the SwiGLU backward and runs
+  // out of registers; the streaming path is the faster one here
   const int path = (N <= 256) ? 1 : 0;
   return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
 }
@@ -324,7 +332,7 @@ int fp8moe_gmm_dlhs_dswiglu_fp8_path(const void* dout, int64_t M, int64_t N, con
                                      const float* scale, int32_t E, int64_t F, const void* gu,
                                      const int32_t* group_sizes, void* dgu, int32_t path,
                                      fp8moe_stream_t stream) {
-  if (path != 0 && path != 1) return FP8MOE_EINVAL;
+  if (path < 0 || path > 2) return FP8MOE_EINVAL;
   if (M > 0 && !gu) return FP8MOE_EINVAL;
   return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
 }

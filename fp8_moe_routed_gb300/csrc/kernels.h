@@ -41,7 +41,8 @@ cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStr
 
 struct GmmDlhsArgs {
   CUtensorMap tmA;        // dout [M, N] bf16 tiles
-  CUtensorMap tmC;        // codes [E, K, N] u8 tiles
+  CUtensorMap tmC;        // codes [E, K, N] u8 tiles [256 k x 64 n], no swizzle
+  CUtensorMap tmCp;       // the same codes as [128 k x 64 n] tiles, 64-byte swizzle (pair path)
   const float* scale;     // [E, N]
   const int32_t* gs;
   const void* gu;         // bf16 [M, 2K] wi output (gate | up) for the dSwiGLU epilogue, or null
@@ -49,8 +50,9 @@ struct GmmDlhsArgs {
   int64_t M;
   int N, K, E;
 };
-cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int cached,
-                                   cudaStream_t s);
+// path: 0 streaming, 1 on-chip weight cache (N <= 256), 2 CTA pairs with the
+// dequantized weight in tensor memory.
+cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int path, cudaStream_t s);
 
 struct TgmmArgs {
   CUtensorMap tmX;        // qx slots [S, 128, K] u8

@@ -122,7 +122,10 @@ int fp8moe_gmm_dlhs_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* c
 /* Same as fp8moe_gmm_dlhs_fp8 with the internal path forced: path 0 streams
  * and dequantizes every weight tile per output tile; path 1 keeps the
  * dequantized weight block of an (expert, k tile) on chip across the expert's
- * m tiles (needs N <= 256, else FP8MOE_EINVAL).  Both give identical bits. */
+ * m tiles (needs N <= 256, else FP8MOE_EINVAL); path 2 computes the transposed
+ * product on CTA pairs with the dequantized weight tile held in tensor memory
+ * (the default for N > 256).  Any other path: FP8MOE_EINVAL.  All paths give
+ * identical bits. */
 int fp8moe_gmm_dlhs_fp8_path(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
                              const float* scale, int32_t E, int64_t K,
                              const int32_t* group_sizes, void* dlhs, int32_t path,
@@ -145,7 +148,8 @@ int fp8moe_gmm_dlhs_dswiglu_fp8(const void* dout, int64_t M, int64_t N, const ui
                                 size_t workspace_bytes, fp8moe_stream_t stream);
 
 /* fp8moe_gmm_dlhs_dswiglu_fp8 with the internal path forced (0 streaming,
- * 1 on-chip weight cache, N <= 256); both give identical bits. */
+ * 1 on-chip weight cache, N <= 256, 2 CTA pairs with the weight in tensor
+ * memory); all give identical bits. */
 int fp8moe_gmm_dlhs_dswiglu_fp8_path(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
                                      const float* scale, int32_t E, int64_t F, const void* gu,
                                      const int32_t* group_sizes, void* dgu, int32_t path,

@@ -61,6 +61,8 @@ def test_argument_checks_run_before_any_device_call():
     P = ctypes.c_void_p
     assert L.fp8moe_gmm_dlhs_fp8_path(P(16), 64, 512, P(16), P(16), 4, 256, P(16), P(16), 1,
                                       None) == -1     # cached path needs N <= 256
+    assert L.fp8moe_gmm_dlhs_fp8_path(P(16), 64, 512, P(16), P(16), 4, 256, P(16), P(16), 3,
+                                      None) == -1     # paths are 0, 1, 2
     assert L.fp8moe_dequantize_fp8_codes(P(16), P(16), 4, 256, 8, P(16), None) == -2
     # argument checks of the entry points added for the next steps of the path
     assert L.fp8moe_selftest_wait_timeout(0, None) == -1              # limit must be > 0

@@ -137,8 +137,8 @@ def test_dropless_tgmm_blocks_finite_and_tail_blind(orc):
 @pytest.mark.parametrize("M", [8192, 131072])
 def test_sweep_forward_and_dlhs_paths(orc, M):
     """E=128, K=4096, F=1536: FP8 wi forward vs the oracle (sampled rows) and vs
-    the BF16 comparison GMM on the same inputs; dLHS with the streaming path
-    (contraction 3072) and the cached path (contraction 256, forward N=256)."""
+    the BF16 comparison GMM on the same inputs; dLHS with the pair and streaming
+    paths (contraction 3072) and the cached path (contraction 256, forward N=256)."""
     E, K, F = 128, 4096, 1536
     gs = W.group_sizes("sweep", seed=3, E=E, M=M)
     gsd = gs.to(DEV)
@@ -155,19 +155,23 @@ def test_sweep_forward_and_dlhs_paths(orc, M):
     rel = ((hb.float() - h.float()).norm() / hb.float().norm()).item()
     assert rel < 0.1, rel
     del w_bf, hb
-    # dLHS streaming (N = 3072)
+    # dLHS, contraction N = 3072: the default (CTA-pair) path against the oracle
+    # on sampled rows and bit for bit against the streaming path
     dgu = W.cotangent(M, 2 * F, 23, device=DEV)
     dx = fb.gmm_dlhs_fp8(dgu, wi_c, wi_s, gsd)
     rows_b = rows[:: max(1, len(rows) // 12)]
     ref_dx, _, bad = orc.gmm_dlhs(dgu.cpu(), wi_c.cpu(), wi_s.cpu(), gs, rows=rows_b)
     assert bad == 0
-    check_bf16(dx.cpu()[rows_b], ref_dx[rows_b], what="sweep dlhs streaming")
+    check_bf16(dx.cpu()[rows_b], ref_dx[rows_b], what="sweep dlhs pair")
+    T = int(gs.sum())
+    dx0 = fb.gmm_dlhs_fp8(dgu, wi_c, wi_s, gsd, path=0)
+    assert torch.equal(bits16(dx[:T]), bits16(dx0[:T])), "pair and streaming paths differ"
+    del dx0
     # dLHS cached (contraction 256) equals streaming bit for bit, and the oracle
     c2, s2 = W.fp8_weights(E, K, 256, 0.02, 24, device=DEV)
     d2 = W.cotangent(M, 256, 25, device=DEV)
     a = fb.gmm_dlhs_fp8(d2, c2, s2, gsd, path=1)
     b = fb.gmm_dlhs_fp8(d2, c2, s2, gsd, path=0)
-    T = int(gs.sum())
     assert torch.equal(bits16(a[:T]), bits16(b[:T]))
     ref_a, _, bad = orc.gmm_dlhs(d2.cpu(), c2.cpu(), s2.cpu(), gs, rows=rows_b)
     assert bad == 0

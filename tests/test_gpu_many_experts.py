@@ -76,7 +76,7 @@ def test_many_experts_gmm_fwd(orc, silu):
     assert (out[T:].float() == 7.0).all(), "rows >= T were written"
 
 
-def test_many_experts_dlhs_both_paths(orc):
+def test_many_experts_dlhs_all_paths(orc):
     N, K = 256, 384
     gs = group_sizes()
     T = int(gs.sum())
@@ -92,6 +92,9 @@ def test_many_experts_dlhs_both_paths(orc):
     out1 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
     fb.gmm_dlhs_fp8(*args, out=out1, path=1)
     assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
+    out2 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out2, path=2)
+    assert torch.equal(bits16(out2), bits16(out0)), "pair and streaming paths differ"
 
 
 def test_many_experts_tgmm(orc):

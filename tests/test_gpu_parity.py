@@ -161,6 +161,38 @@ def test_dlhs_vs_oracle_and_paths_identical(orc, M, N, K, E, gs):
         out1 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
         fb.gmm_dlhs_fp8(*args, out=out1, path=1)
         assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
+    # CTA pairs with the dequantized weight in tensor memory: the same bits
+    out2 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out2, path=2)
+    assert torch.equal(bits16(out2), bits16(out0)), "pair and streaming paths differ"
+
+
+PAIR_CASES = [
+    (800, 320, 384, 3, [130, 0, 300]),                # k tile of 128 past K = 384
+    (600, 176, 272, 2, [100, 200]),                   # N % 64 = 48, K % 256 = 16
+    (1100, 4096, 512, 4, [1, 255, 257, 512]),         # one-row group, 257 = 256 + 1
+]
+
+
+@pytest.mark.parametrize("M,N,K,E,gs", PAIR_CASES)
+def test_dlhs_pair_path_edges(orc, M, N, K, E, gs):
+    """The CTA-pair path (256 weight rows x 256 token rows per unit) on the
+    shapes where its tiling is ragged: against the oracle and bit for bit
+    against the streaming path; rows past T untouched."""
+    gs = torch.tensor(gs, dtype=torch.int32)
+    T = int(gs.sum())
+    dout = W.fill_tail_garbage(W.cotangent(M, N, seed=N + 7), T)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=K + 7)
+    args = cuda(dout, codes, scale, gs)
+    out2 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out2, path=2)
+    ref, _, bad = orc.gmm_dlhs(dout, codes, scale, gs)
+    assert bad == 0
+    check_bf16(out2[:T], ref[:T], what="dlhs pair path")
+    assert (out2[T:].float() == 7.0).all(), "rows >= T were written"
+    out0 = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(*args, out=out0, path=0)
+    assert torch.equal(bits16(out2), bits16(out0)), "pair and streaming paths differ"
 
 
 # ---------------------------------------------------- wo dLHS + dSwiGLU
@@ -191,7 +223,10 @@ def test_dlhs_dswiglu_vs_oracle_and_paths_identical(orc, M, N, F, E, gs):
         out1 = torch.full((M, 2 * F), 7.0, dtype=torch.bfloat16, device=DEV)
         fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg, out=out1, path=1)
         assert torch.equal(bits16(out1), bits16(out0)), "cached and streaming paths differ"
-    # the default entry point picks one of the two paths
+    out3 = torch.full((M, 2 * F), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg, out=out3, path=2)
+    assert torch.equal(bits16(out3), bits16(out0)), "pair and streaming paths differ"
+    # the default entry point picks one of the paths
     out2 = fb.gmm_dlhs_dswiglu_fp8(dg, cg, sg, gug, gsg)
     assert torch.equal(bits16(out2[:T]), bits16(out0[:T]))
 
