@@ -608,8 +608,8 @@ cudaError_t launch(const GmmDlhsArgs& a, int num_sms, cudaStream_t s) {
 //                trip) is longer than a step of MMAs, so each warp gets four
 //                steps' time for it.
 // setmaxnreg moves registers from the first warpgroup (32 each) and the dequant
-// warps (48) to the epilogue warps (136), which hold a 128-column half of the
-// accumulator.
+// warps (56) to the epilogue warps (120), which hold a 128-column half of the
+// accumulator as bf16 pairs.
 // Publishing the odd CTA's A half to the even CTA's MMA: each dequant thread
 // blocks in tcgen05.wait::st until its TMEM stores have completed, then its
 // warp arrives on the even CTA's barrier. A cluster-scope release on that
@@ -642,8 +642,8 @@ constexpr int kFirstEpi = kCtlWarps, kFirstDq = kCtlWarps + kEpiWarps;
 constexpr int kThreads = (kCtlWarps + kEpiWarps + kDqWarps) * 32;   // 896
 // 72 registers a thread at launch (65536 / 896, rounded down to 8); afterwards
 // each SM sub-partition holds one warp of every warpgroup, so the shares must
-// stay within 7 x 72 per sub-partition: 32 + 2 x 136 + 4 x 48 = 496.
-constexpr int kCtlRegs = 32, kEpiRegs = 136, kDqRegs = 48;
+// stay within 7 x 72 per sub-partition: 32 + 2 x 120 + 4 x 56 = 496.
+constexpr int kCtlRegs = 32, kEpiRegs = 120, kDqRegs = 56;
 static_assert(kCtlRegs + 2 * kEpiRegs + 4 * kDqRegs <= 7 * 72, "register hand-over");
 
 struct Smem {
@@ -864,26 +864,18 @@ gmm_dlhs_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
       tc_fence_after();
       // the whole 128-column half in registers, as bf16 pairs (DSW: f32)
       uint32_t v[DSW ? 128 : 64];
-      // two 32-column loads in flight per wait
 #pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t w0[32], w1[32];
-        tmem_ld32(tbase + c * 32, w0);
-        tmem_ld32(tbase + c * 32 + 32, w1);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[32];
+        tmem_ld32(tbase + c * 32, w);
         tmem_ld_wait();
         if (DSW) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[c * 32 + i] = w0[i];
-            v[c * 32 + 32 + i] = w1[i];
-          }
+          for (int i = 0; i < 32; ++i) v[c * 32 + i] = w[i];
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[c * 16 + i] = f32x2_to_bf16x2(__uint_as_float(w0[2 * i]), __uint_as_float(w0[2 * i + 1]));
-            v[c * 16 + 16 + i] =
-                f32x2_to_bf16x2(__uint_as_float(w1[2 * i]), __uint_as_float(w1[2 * i + 1]));
-          }
+          for (int i = 0; i < 16; ++i)
+            v[c * 16 + i] = f32x2_to_bf16x2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
         }
       }
       tc_fence_before();
@@ -942,21 +934,28 @@ gmm_dlhs_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         tc_fence_after();
         const uint8_t* crow = c_tile(st) + r * 64;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 c = *reinterpret_cast<const uint4*>(crow + ((j ^ x) << 4));
-          // N % 16 == 0: a 16-column group is fully in range or fully out (past
-          // N the slot holds an earlier step's scales and the codes are zero)
-          float sc[16];
-          const bool in = kb * kBK + j * 16 < N;
-          const float4* p = reinterpret_cast<const float4*>(scales + st * kBK + j * 16);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f = in ? p[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            sc[4 * q] = f.x; sc[4 * q + 1] = f.y; sc[4 * q + 2] = f.z; sc[4 * q + 3] = f.w;
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * h + jj;
+            const uint4 c = *reinterpret_cast<const uint4*>(crow + ((j ^ x) << 4));
+            // N % 16 == 0: a 16-column group is fully in range or fully out (past
+            // N the slot holds an earlier step's scales and the codes are zero)
+            float sc[16];
+            const bool in = kb * kBK + j * 16 < N;
+            const float4* p = reinterpret_cast<const float4*>(scales + st * kBK + j * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 f = in ? p[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+              sc[4 * q] = f.x; sc[4 * q + 1] = f.y; sc[4 * q + 2] = f.z; sc[4 * q + 3] = f.w;
+            }
+            uint32_t oj[8];
+            dequant16(c, sc, oj);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[8 * jj + q] = oj[q];
           }
-          uint32_t o[8];
-          dequant16(c, sc, o);
-          tmem_st8(tcol + (uint32_t)(as * kACols + j * 8), o);
+          tmem_st16(tcol + (uint32_t)(as * kACols + h * 16), o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.sempty[st]);   // codes and scales read
