@@ -10,6 +10,16 @@
 // dequantized block is also kept on chip across the expert's m tiles (the
 // review thread on the cache: it only hits with one K tile).
 //
+// Three kernels, all giving the same bits:
+//   gmm_dlhs_pair_kernel (end of this file) -- the default for contractions
+//     past 256: CTA pairs, the product transposed, the dequantized weight tile
+//     written into tensor memory as the MMA's A operand;
+//   gmm_dlhs_kernel<CACHED = true> -- contractions up to 256: the dequantized
+//     weight block cached in shared memory across a run of m tiles;
+//   gmm_dlhs_kernel<CACHED = false> -- streaming, kept as the dSwiGLU default
+//     (its epilogue reads f32 accumulators chunk by chunk, which the pair
+//     kernel's registers do not allow) and as a forced path.
+//
 // GB300 design (one CTA per SM, persistent), per 128-row x 256-column output
 // tile and 64-wide contraction step:
 //   warp 0       TMA: dout tiles [128 x 64] bf16 (K-major, 128-byte swizzle) and
