@@ -48,6 +48,13 @@ METRIC = "FP8 GMM TFLOP/s (wi+SwiGLU fwd, wo fwd, dLHS) and % of GB300 FP8 peak"
 WI_FWD_TRAFFIC = 2088.2e6
 WI_FWD_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi forward "
                          "(row quantizer + GMM), profiles/gmm_fwd_wi_e4_m4096_k7168_n4096.md")
+# DRAM bytes (read + write) of one wi dLHS launch (gmm_dlhs_pair_kernel<0>,
+# contraction 4096, output 7168) at 32 experts x 1024 rows: 1355.6 + 456.8 MB,
+# from a one-pass ncu capture of this bench's workload. Valid for that kernel
+# as captured; set to None when it changes.
+WI_DLHS_TRAFFIC = 1812.4e6
+WI_DLHS_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi dLHS "
+                          "launch, profiles/gmm_dlhs_pair_e4_m4096.md")
 
 
 def step_flops(T: int) -> dict:
@@ -403,6 +410,7 @@ def main():
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16"]            # fp8 dense = 2 x bf16 dense (nominal ratio)
     wi_tflops = flops["wi_fwd"] / (per["wi_fwd"] * 1e-3) / 1e12
+    dl_tflops = flops["wi_dlhs"] / (per["wi_dlhs"] * 1e-3) / 1e12
     kern = {}
     for n in names:
         tf = flops[n] / (per[n] * 1e-3) / 1e12
@@ -557,12 +565,22 @@ def main():
                        "l2": "inputs larger than L2 (~5 GB streamed per step), no flush",
                        "parallelism": f"replicas x{world} (expert-parallel shards)"},
             "gpu_launches": step.launches_per_step * K,
-            "roofline": {"kernel": "wi fwd (row quantize + FP8 GMM + SwiGLU)", "bound": "tensor",
-                         "achieved": round(wi_tflops, 1), "peak": round(fp8_peak, 1),
-                         "unit": "TFLOP/s", "frac": round(wi_tflops / fp8_peak, 3),
-                         "traffic": WI_FWD_TRAFFIC if E == 32 else None,
-                         "traffic_source": WI_FWD_TRAFFIC_SOURCE if E == 32 else None,
-                         "peak_source": f"{pk['source']} bf16 x2 (fp8/bf16 nominal ratio), burst"},
+            # the dominant kernel by time: the dLHS (two launches, half the step);
+            # its larger launch is the wi dLHS
+            "roofline": {"kernel": "wi dLHS (gmm_dlhs_pair_kernel: CTA pairs, dequantized weight in TMEM)",
+                         "bound": "tensor", "achieved": round(dl_tflops, 1),
+                         "peak": round(pk["bf16"], 1), "unit": "TFLOP/s",
+                         "frac": round(dl_tflops / pk["bf16"], 3),
+                         "traffic": WI_DLHS_TRAFFIC if E == 32 else None,
+                         "traffic_source": WI_DLHS_TRAFFIC_SOURCE if E == 32 and WI_DLHS_TRAFFIC else None,
+                         "peak_source": f"{pk['source']} bf16, burst"},
+            # the row the pages' target is set on: the wi forward with its quantization
+            "roofline_wi_fwd": {"kernel": "wi fwd (row quantize + FP8 GMM + SwiGLU)", "bound": "tensor",
+                                "achieved": round(wi_tflops, 1), "peak": round(fp8_peak, 1),
+                                "unit": "TFLOP/s", "frac": round(wi_tflops / fp8_peak, 3),
+                                "traffic": WI_FWD_TRAFFIC if E == 32 else None,
+                                "traffic_source": WI_FWD_TRAFFIC_SOURCE if E == 32 else None,
+                                "peak_source": f"{pk['source']} bf16 x2 (fp8/bf16 nominal ratio), burst"},
             "kernels": kern, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, **extra,
         }
         print(json.dumps(line), flush=True)
