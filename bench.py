@@ -342,14 +342,15 @@ def main():
     if args.experts != E:
         E = args.experts
         M = E * ROWS_PER_EXPERT
-    world, rank, local = dist_setup(args)
     T = M
     flops = step_flops(T)
     total_flops = sum(flops.values())
 
     if args.impl == "reference":
         # The reference arm is the CPU oracle (the pages publish no runnable code).
-        if rank != 0:
+        # Rank 0 alone runs it; it needs no process group, so the other ranks of
+        # a torchrun launch exit at once.
+        if int(os.environ.get("RANK", "0")) != 0:
             return
         times = []
         vals = []
@@ -371,6 +372,7 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    world, rank, local = dist_setup(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     from fp8_moe_routed_gb300 import binding as fb

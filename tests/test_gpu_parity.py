@@ -197,9 +197,9 @@ def test_dlhs_pair_path_edges(orc, M, N, K, E, gs):
 
 # ---------------------------------------------------- wo dLHS + dSwiGLU
 DSWIGLU_CASES = [
-    (512, 256, 128, 4, "tiny"),                       # N <= 256: both paths
+    (512, 256, 128, 4, "tiny"),                       # N <= 256: all three paths
     (1024, 512, 272, 3, [300, 0, 500]),               # F = 272: partial column chunk
-    (640, 160, 64, 2, [0, 600]),                      # first expert empty, both paths
+    (640, 160, 64, 2, [0, 600]),                      # first expert empty, all three paths
 ]
 
 
