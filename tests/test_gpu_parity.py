@@ -195,6 +195,25 @@ def test_dlhs_pair_path_edges(orc, M, N, K, E, gs):
     assert torch.equal(bits16(out2), bits16(out0)), "pair and streaming paths differ"
 
 
+def test_dlhs_all_groups_empty_every_path():
+    """No rows at all (every group empty, M > 0): each dLHS path launches, finds
+    no work unit, writes nothing and leaves the status word clean."""
+    M, N, K, E = 96, 320, 256, 3
+    gs = torch.zeros(E, dtype=torch.int32, device=DEV)
+    dout = torch.randn(M, N, device=DEV).to(torch.bfloat16)
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=9, device=DEV)
+    for path in (0, 2):
+        out = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+        fb.gmm_dlhs_fp8(dout, codes, scale, gs, out=out, path=path)
+        torch.cuda.synchronize()
+        assert (out.float() == 7.0).all(), f"path {path} wrote rows of empty groups"
+    c1, s1 = W.fp8_weights(E, K, 256, 0.02, seed=10, device=DEV)
+    out = torch.full((M, K), 7.0, dtype=torch.bfloat16, device=DEV)
+    fb.gmm_dlhs_fp8(dout[:, :256].contiguous(), c1, s1, gs, out=out, path=1)
+    torch.cuda.synchronize()
+    assert (out.float() == 7.0).all(), "path 1 wrote rows of empty groups"
+
+
 # ---------------------------------------------------- wo dLHS + dSwiGLU
 DSWIGLU_CASES = [
     (512, 256, 128, 4, "tiny"),                       # N <= 256: all three paths
