@@ -111,7 +111,9 @@ int fp8moe_gmm_silu_fp8_fwd(const void* lhs, int64_t M, int64_t K, const uint8_t
  * (rhs_contract_dequant): each weight tile is dequantized on chip,
  *   w[e,k,n] = bf16(f32(codes[e,k,n]) * scale[e,n]),
  *   dlhs[m,k] = bf16( sum_n dout[m,n] * w[e,k,n] )   (f32 accumulation),
- * bit-identical whichever internal path (cached or streaming) is taken.
+ * bit-identical whichever internal path is taken (contraction N <= 256: the
+ * dequantized weight block cached in shared memory; N > 256: CTA pairs with the
+ * dequantized weight tile in tensor memory).
  * dout: bf16 [M, N] (the forward output's cotangent).  dlhs: bf16 [M, K];
  * rows >= T untouched.  No workspace (pass NULL, 0). */
 int fp8moe_gmm_dlhs_fp8(const void* dout, int64_t M, int64_t N, const uint8_t* codes,
