@@ -322,8 +322,8 @@ int fp8moe_gmm_dlhs_dswiglu_fp8(const void* dout, int64_t M, int64_t N, const ui
   (void)workspace;
   (void)workspace_bytes;
   if (M > 0 && !gu) return FP8MOE_EINVAL;
-  // the pair path's epilogue holds f32 values for the SwiGLU backward and runs
-  // out of registers; the streaming path is the faster one here
+  // the pair path has one accumulator and must hold it through the SwiGLU
+  // backward, which stalls its MMAs; the streaming path is the faster one here
   const int path = (N <= 256) ? 1 : 0;
   return dlhs_impl(dout, M, N, codes, scale, E, F, group_sizes, gu, dgu, path, stream);
 }

@@ -17,8 +17,9 @@
 //   gmm_dlhs_kernel<CACHED = true> -- contractions up to 256: the dequantized
 //     weight block cached in shared memory across a run of m tiles;
 //   gmm_dlhs_kernel<CACHED = false> -- streaming, kept as the dSwiGLU default
-//     (its epilogue reads f32 accumulators chunk by chunk, which the pair
-//     kernel's registers do not allow) and as a forced path.
+//     (two accumulators let its SwiGLU epilogue overlap the next tile's MMAs;
+//     the pair kernel has one and must hold it through the SwiGLU math) and as
+//     a forced path.
 //
 // GB300 design (one CTA per SM, persistent), per 128-row x 256-column output
 // tile and 64-wide contraction step:
@@ -870,53 +871,88 @@ gmm_dlhs_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint32_t tph = 0;
     for (int u = cluster; u < total; u += nclusters) {
       const Unit t = decode_unit(s, E, nkt, u);
+      const int k = t.k0 + rank * kRows + r;
+      const int jn = min(128, t.rows - half * 128);   // valid token rows of this half
+      const int64_t row0 = (int64_t)t.m0 + half * 128;
+      if (DSW) {
+        // dSwiGLU needs the f32 accumulator, 128 values a thread: too many to hold
+        // in registers, so the epilogue works through the accumulator 16 columns
+        // at a time while holding it, loading each chunk's g and u one chunk ahead
+        // (the first chunk's before the accumulator is ready)
+        const bool kin = k < K;
+        const uint16_t* gub = reinterpret_cast<const uint16_t*>(gu) + row0 * 2 * K + k;
+        uint16_t* ob = reinterpret_cast<uint16_t*>(dlhs) + row0 * 2 * K + k;
+        auto fetch = [&](int c, uint32_t (&g)[16], uint32_t (&uu)[16]) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int jj = c * 16 + j;
+            g[j] = 0u;
+            uu[j] = 0u;
+            if (kin && jj < jn) {
+              g[j] = __ldg(gub + (int64_t)jj * 2 * K);
+              uu[j] = __ldg(gub + (int64_t)jj * 2 * K + K);
+            }
+          }
+        };
+        uint32_t g0[16], u0[16];
+        fetch(0, g0, u0);
+        if (!mbar_wait_warp_cluster(&s.tfull, tph, kWhereEpilogue)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t g1[16], u1[16];
+          if (c + 1 < 8) fetch(c + 1, g1, u1);
+          uint32_t w[16];
+          tmem_ld16(tbase + c * 16, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int jj = c * 16 + j;
+            if (kin && jj < jn) {
+              uint16_t dg, du;
+              dswiglu1(__uint_as_float(w[j]), (uint16_t)g0[j], (uint16_t)u0[j], dg, du);
+              ob[(int64_t)jj * 2 * K] = dg;
+              ob[(int64_t)jj * 2 * K + K] = du;
+            }
+          }
+          if (c + 1 < 8) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              g0[j] = g1[j];
+              u0[j] = u1[j];
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&s.tempty), 0));
+        tph ^= 1;
+        continue;
+      }
       if (!mbar_wait_warp_cluster(&s.tfull, tph, kWhereEpilogue)) break;
       tc_fence_after();
-      // the whole 128-column half in registers, as bf16 pairs (DSW: f32)
-      uint32_t v[DSW ? 128 : 64];
+      // the whole 128-column half in registers as bf16 pairs
+      uint32_t v[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[32];
         tmem_ld32(tbase + c * 32, w);
         tmem_ld_wait();
-        if (DSW) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[c * 32 + i] = w[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            v[c * 16 + i] = f32x2_to_bf16x2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
-        }
+        for (int i = 0; i < 16; ++i)
+          v[c * 16 + i] = f32x2_to_bf16x2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
       }
       tc_fence_before();
       __syncwarp();
       // the even CTA's MMA thread waits for the epilogue warps of both CTAs
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&s.tempty), 0));
       tph ^= 1;
-      const int k = t.k0 + rank * kRows + r;
-      const int jn = min(128, t.rows - half * 128);   // valid token rows of this half
       if (k < K && jn > 0) {
-        const int64_t row0 = (int64_t)t.m0 + half * 128;
-        if (DSW) {
-          const uint16_t* gub = reinterpret_cast<const uint16_t*>(gu) + row0 * 2 * K + k;
-          uint16_t* ob = reinterpret_cast<uint16_t*>(dlhs) + row0 * 2 * K + k;
+        uint16_t* ob = reinterpret_cast<uint16_t*>(dlhs) + row0 * K + k;
 #pragma unroll
-          for (int j = 0; j < 128; ++j) {
-            if (j < jn) {
-              uint16_t dg, du;
-              dswiglu1(__uint_as_float(v[j]), __ldg(gub + (int64_t)j * 2 * K),
-                       __ldg(gub + (int64_t)j * 2 * K + K), dg, du);
-              ob[(int64_t)j * 2 * K] = dg;
-              ob[(int64_t)j * 2 * K + K] = du;
-            }
-          }
-        } else {
-          uint16_t* ob = reinterpret_cast<uint16_t*>(dlhs) + row0 * K + k;
-#pragma unroll
-          for (int j = 0; j < 128; ++j) {
-            if (j < jn) *ob = (uint16_t)(v[j >> 1] >> (16 * (j & 1)));
-            ob += K;
-          }
+        for (int j = 0; j < 128; ++j) {
+          if (j < jn) *ob = (uint16_t)(v[j >> 1] >> (16 * (j & 1)));
+          ob += K;
         }
       }
     }
