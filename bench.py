@@ -49,10 +49,10 @@ WI_FWD_TRAFFIC = 2088.2e6
 WI_FWD_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi forward "
                          "(row quantizer + GMM), profiles/gmm_fwd_wi_e4_m4096_k7168_n4096.md")
 # DRAM bytes (read + write) of one wi dLHS launch (gmm_dlhs_pair_kernel<0>,
-# contraction 4096, output 7168) at 32 experts x 1024 rows: 1355.6 + 456.8 MB,
+# contraction 4096, output 7168) at 32 experts x 1024 rows: 1341.5 + 457.2 MB,
 # from a one-pass ncu capture of this bench's workload. Valid for that kernel
 # as captured; set to None when it changes.
-WI_DLHS_TRAFFIC = 1812.4e6
+WI_DLHS_TRAFFIC = 1798.7e6
 WI_DLHS_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, full-size wi dLHS "
                           "launch, profiles/gmm_dlhs_pair_e4_m4096.md")
 
