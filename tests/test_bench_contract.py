@@ -48,3 +48,35 @@ def test_reference_arm_other_ranks_do_no_work():
               "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": "1"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert not [l for l in p.stdout.splitlines() if l.startswith("{")]
+
+
+def test_summarize_launches_groups_units_and_shares(tmp_path):
+    """The launch-list summary behind the committed profiles: ncu's preamble
+    lines are skipped, launches group by kernel name (template arguments kept,
+    parameter list dropped), times in ns / us / ms all come out in us, and the
+    shares add up to 1."""
+    import bench
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"')
+
+    def row(i, name, unit, value):
+        return (f'"{i}","1","python3","host","{name}","1","7","(896, 1, 1)","(152, 1, 1)","0",'
+                f'"10.3","Command line profiler metrics","gpu__time_duration.sum","{unit}","{value}"')
+
+    lines = ["==PROF== Connected to process 1", hdr,
+             row(0, "void k::a<0>(int, float *)", "usecond", "300"),
+             row(1, "void k::b(int)", "nsecond", "100,000"),
+             row(2, "void k::a<0>(int, float *)", "msecond", "0.5"),
+             row(3, "void k::a<1>(int, float *)", "usecond", "100")]
+    p = tmp_path / "launches.csv"
+    p.write_text("\n".join(lines) + "\n")
+    table = bench.summarize_launches(str(p)).splitlines()
+    assert table[0].startswith("| kernel | launches")
+    body = [[c.strip() for c in l.strip("|").split("|")] for l in table[2:]]
+    names = [b[0] for b in body]
+    assert names == ["`void k::a<0>`", "`void k::b`", "`void k::a<1>`"]   # by total time
+    a0 = body[0]
+    assert a0[1] == "2" and float(a0[2]) == 800.0 and float(a0[3]) == 400.0
+    assert float(body[1][2]) == 100.0 and float(body[2][2]) == 100.0
+    assert abs(sum(float(b[4]) for b in body) - 1.0) < 2e-3
