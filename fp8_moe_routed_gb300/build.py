@@ -17,8 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libfp8moe.so")
 
-SOURCES = ["api.cu", "quant.cu", "dequant.cu", "gmm_fwd.cu", "gmm_dlhs.cu", "tgmm.cu",
-           "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "quant.cu", "dequant.cu", "gmm_fwd.cu", "gmm_dlhs.cu", "gmm_dlhs_pair.cu",
+           "tgmm.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

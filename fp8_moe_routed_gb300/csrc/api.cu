@@ -614,7 +614,8 @@ int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags) {
   uint32_t v = 0;
   uint32_t (*takes[])(cudaStream_t) = {fp8moe_status_take_quant, fp8moe_status_take_dequant,
                                        fp8moe_status_take_gmm_fwd, fp8moe_status_take_dlhs,
-                                       fp8moe_status_take_tgmm, fp8moe_status_take_selftest};
+                                       fp8moe_status_take_dlhs_pair, fp8moe_status_take_tgmm,
+                                       fp8moe_status_take_selftest};
   for (auto take : takes) {
     uint32_t x = take(stream);
     if (x == 0xFFFFFFFFu) return cuda_fail(cudaGetLastError());

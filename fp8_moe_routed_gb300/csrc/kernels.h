@@ -53,6 +53,8 @@ struct GmmDlhsArgs {
 // path: 0 streaming, 1 on-chip weight cache (N <= 256), 2 CTA pairs with the
 // dequantized weight in tensor memory.
 cudaError_t fp8moe_launch_gmm_dlhs(const GmmDlhsArgs& a, int num_sms, int path, cudaStream_t s);
+// The pair kernel alone (gmm_dlhs_pair.cu); fp8moe_launch_gmm_dlhs routes path 2 here.
+cudaError_t fp8moe_launch_gmm_dlhs_pair(const GmmDlhsArgs& a, int num_sms, cudaStream_t s);
 
 struct TgmmArgs {
   CUtensorMap tmX;        // qx slots [S, 128, K] u8
@@ -75,6 +77,7 @@ uint32_t fp8moe_status_take_quant(cudaStream_t s);
 uint32_t fp8moe_status_take_dequant(cudaStream_t s);
 uint32_t fp8moe_status_take_gmm_fwd(cudaStream_t s);
 uint32_t fp8moe_status_take_dlhs(cudaStream_t s);
+uint32_t fp8moe_status_take_dlhs_pair(cudaStream_t s);
 uint32_t fp8moe_status_take_tgmm(cudaStream_t s);
 uint32_t fp8moe_status_take_selftest(cudaStream_t s);
 
