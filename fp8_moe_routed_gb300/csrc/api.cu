@@ -641,6 +641,27 @@ int fp8moe_last_cuda_error(void) { return t_last_cuda_error; }
 
 void fp8moe_internal_set_cuda_error(int e) { t_last_cuda_error = e; }
 
+// The forward's argument checks that come before its workspace check, in the
+// same order and with the same codes (for callers that supply the workspace
+// themselves). FP8MOE_OK with *empty = 1: M == 0, nothing to do.
+int fp8moe_internal_check_fwd_args(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
+                                   const float* scale, int32_t E, int64_t N, const int32_t* gs,
+                                   const void* out, int swiglu, int* empty) {
+  *empty = 0;
+  int rc = check_common(M, K, N, E);
+  if (rc) return rc;
+  if (swiglu && (N % 32 != 0)) return FP8MOE_EALIGN;
+  if (M == 0) {
+    *empty = 1;
+    return FP8MOE_OK;
+  }
+  if (!lhs || !codes || !scale || !gs || !out) return FP8MOE_EINVAL;
+  if (!aligned16(lhs) || !aligned16(codes) || !aligned16(scale) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(gs) & 3u))
+    return FP8MOE_EALIGN;
+  return FP8MOE_OK;
+}
+
 int fp8moe_num_sms(void) {
   int sms = 0;
   if (device_init(&sms) != FP8MOE_OK) return 0;

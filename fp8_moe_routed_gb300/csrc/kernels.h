@@ -72,6 +72,10 @@ cudaError_t fp8moe_launch_tgmm(const TgmmArgs& a, int num_sms, cudaStream_t s);
 
 // Records the CUDA error that fp8moe_last_cuda_error() reports (api.cu).
 extern "C" void fp8moe_internal_set_cuda_error(int e);
+extern "C" int fp8moe_internal_check_fwd_args(const void* lhs, int64_t M, int64_t K,
+                                              const uint8_t* codes, const float* scale, int32_t E,
+                                              int64_t N, const int32_t* gs, const void* out,
+                                              int swiglu, int* empty);
 
 uint32_t fp8moe_status_take_quant(cudaStream_t s);
 uint32_t fp8moe_status_take_dequant(cudaStream_t s);

@@ -17,6 +17,12 @@
 // (different streams, no ordering between them) race on it. Every call fully
 // rewrites what it later reads (codes and scales of the rows it covers), so no
 // contents need clearing between calls.
+//
+// The array's device address is looked up once per device and kept. A
+// cudaDeviceReset (or anything else that tears down and re-creates the
+// device's primary context) reloads the module, possibly elsewhere, and leaves
+// the kept address dangling: do not call this entry point again in a process
+// after resetting the device.
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
@@ -43,6 +49,12 @@ extern "C" int fp8moe_gmm_silu_fp8_fwd_noalloc(const void* lhs, int64_t M, int64
                                                 int32_t E, int64_t N,
                                                 const int32_t* group_sizes, void* out,
                                                 fp8moe_stream_t stream) {
+  // the regular entry point's argument checks first, so that a bad argument
+  // gets the same code here as there, whatever the size
+  int empty = 0;
+  int rc = fp8moe_internal_check_fwd_args(lhs, M, K, codes, scale, E, N, group_sizes, out, 1,
+                                          &empty);
+  if (rc != FP8MOE_OK || empty) return rc;
   const size_t need = fp8moe_workspace_size(FP8MOE_OP_GMM_SILU_FP8_FWD, M, K, N, E);
   if (need > kNoAllocScratchBytes) return FP8MOE_EWORKSPACE;
   int dev = 0;

@@ -202,3 +202,42 @@ MICROBENCH = Shapes("microbench", E=64, K=4096, F=1024, M=225280, routing="full_
 def sweep_shapes(M: int) -> Shapes:
     return Shapes(f"sweep_M{M}", E=128, K=4096, F=1536, M=M, routing="sweep",
                   sigma_wi=0.02, sigma_wo=0.02)
+
+
+@dataclasses.dataclass(frozen=True)
+class ExpertShard:
+    """One rank's part of an expert-parallel split of the ragged buffer: the
+    experts [e0, e1) and the rows [row0, row1) their groups cover."""
+    rank: int
+    world: int
+    e0: int
+    e1: int
+    row0: int
+    row1: int
+
+    def take(self, gs: torch.Tensor, rows=(), experts=()):
+        """This rank's slice of group_sizes, of every row-indexed tensor in
+        ``rows`` (leading dim = the buffer's rows) and of every expert-indexed
+        tensor in ``experts`` (leading dim = E)."""
+        return (gs[self.e0:self.e1].contiguous(),
+                [t[self.row0:self.row1] for t in rows],
+                [t[self.e0:self.e1] for t in experts])
+
+
+def expert_shard(gs: torch.Tensor, rank: int, world: int, M: Optional[int] = None) -> ExpertShard:
+    """Expert parallelism (each rank owns a contiguous block of the experts, as
+    equal in count as possible, with the rows of their groups). Group sizes are
+    read the way the kernels read them: a negative size counts as 0 and row
+    ranges are clipped at M (default: the sum of the sizes)."""
+    E = gs.numel()
+    if not 0 <= rank < world or world > E:
+        raise ValueError(f"rank {rank} of {world} for {E} experts")
+    e0 = rank * E // world
+    e1 = (rank + 1) * E // world
+    sizes = gs.to(torch.int64).clamp_min(0)
+    off = torch.cat([torch.zeros(1, dtype=torch.int64), sizes.cumsum(0)])
+    total = int(off[-1])
+    M = total if M is None else M
+    row0 = min(int(off[e0]), M)
+    row1 = min(int(off[e1]), M)
+    return ExpertShard(rank, world, e0, e1, row0, row1)

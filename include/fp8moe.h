@@ -258,11 +258,14 @@ int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags);
  * workspace, which comes from a fixed 32 MiB device array that the library holds
  * on every GPU it is loaded on until the process exits; sizes whose workspace
  * (fp8moe_workspace_size(FP8MOE_OP_GMM_SILU_FP8_FWD, ...)) exceeds it return
- * FP8MOE_EWORKSPACE and launch nothing.  The first call on a device looks up the
- * array's device address (make that call before any stream capture).  All calls
- * share the array, so calls that overlap on the GPU race; each call rewrites
- * everything it reads, so nothing needs clearing between calls.  Allocates
- * nothing. */
+ * FP8MOE_EWORKSPACE and launch nothing.  Argument errors are checked first and
+ * return what fp8moe_gmm_silu_fp8_fwd would (FP8MOE_EINVAL, FP8MOE_EALIGN),
+ * whatever the size.  The first call on a device looks up the array's device
+ * address and keeps it (make that call before any stream capture); after a
+ * cudaDeviceReset the kept address is stale, so do not call this again in that
+ * process.  All calls share the array, so calls that overlap on the GPU race;
+ * each call rewrites everything it reads, so nothing needs clearing between
+ * calls.  Allocates nothing. */
 int fp8moe_gmm_silu_fp8_fwd_noalloc(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
                                     const float* scale, int32_t E, int64_t N,
                                     const int32_t* group_sizes, void* out,

@@ -34,7 +34,11 @@ def test_reference_arm_json_line():
     assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
     assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 0
     assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"] == bench.bench_config(1)      # the GPU arm's config, every key
     assert d["config"]["workload"] == "deepseek_v3_moe_balanced"
+    assert "extrapolated" in d["ms_per_step_basis"]
+    om = d["oracle_measured"]
+    assert om["seconds_per_step_sample"] > 0 and om["rows_per_gmm_per_sample"] >= 4
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert isinstance(cb["sample"], str) and cb["sample"]
@@ -80,3 +84,16 @@ def test_summarize_launches_groups_units_and_shares(tmp_path):
     assert a0[1] == "2" and float(a0[2]) == 800.0 and float(a0[3]) == 400.0
     assert float(body[1][2]) == 100.0 and float(body[2][2]) == 100.0
     assert abs(sum(float(b[4]) for b in body) - 1.0) < 2e-3
+
+
+def test_traffic_is_null_unless_captured_on_the_current_sources(monkeypatch):
+    """The roofline traffic figures are tied to a hash of the kernel sources
+    they were measured on: a changed source gives null, not a stale number."""
+    import bench
+    t = dict(bench.TRAFFIC["wi_dlhs"])
+    monkeypatch.setitem(bench.TRAFFIC, "wi_dlhs", dict(t, bytes=1.5e9,
+                                                        sha1=bench.sources_sha1(t["sources"])))
+    assert bench.traffic("wi_dlhs")[0] == 1.5e9
+    monkeypatch.setitem(bench.TRAFFIC, "wi_dlhs", dict(t, bytes=1.5e9, sha1="0" * 40))
+    b, why = bench.traffic("wi_dlhs")
+    assert b is None and "changed" in why

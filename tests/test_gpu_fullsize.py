@@ -134,11 +134,12 @@ def test_dropless_tgmm_blocks_finite_and_tail_blind(orc):
         check_f32_rel(dw[e, kr[0]:kr[1], nr[0]:nr[1]], ref[0], what=f"tgmm e={e}")
 
 
-@pytest.mark.parametrize("M", [8192, 131072])
+@pytest.mark.parametrize("M", [8192, 16384, 32768, 65536, 131072])
 def test_sweep_forward_and_dlhs_paths(orc, M):
-    """E=128, K=4096, F=1536: FP8 wi forward vs the oracle (sampled rows) and vs
-    the BF16 comparison GMM on the same inputs; dLHS with the pair and streaming
-    paths (contraction 3072) and the cached path (contraction 256, forward N=256)."""
+    """E=128, K=4096, F=1536 at every swept M: FP8 wi forward (+SwiGLU) and wo
+    forward (K=1536, N=4096) vs the oracle on sampled rows and vs the BF16
+    comparison GMM on the same inputs; dLHS with the pair and streaming paths
+    (contraction 3072) and the cached path (contraction 256, forward N=256)."""
     E, K, F = 128, 4096, 1536
     gs = W.group_sizes("sweep", seed=3, E=E, M=M)
     gsd = gs.to(DEV)
@@ -155,6 +156,17 @@ def test_sweep_forward_and_dlhs_paths(orc, M):
     rel = ((hb.float() - h.float()).norm() / hb.float().norm()).item()
     assert rel < 0.1, rel
     del w_bf, hb
+    # wo forward on the wi output: K = 1536, N = 4096
+    wo_c, wo_s = W.fp8_weights(E, F, K, 0.02, 26, device=DEV)
+    y = fb.gmm_fp8_fwd(h, wo_c, wo_s, gsd)
+    ref_y, _, bad = orc.gmm_fwd(h.cpu(), wo_c.cpu(), wo_s.cpu(), gs, silu=False, rows=rows)
+    assert bad == 0
+    check_bf16(y.cpu()[rows], ref_y[rows], what="sweep wo fwd")
+    wo_bf = fb.dequantize_fp8_codes(wo_c, wo_s)
+    yb = fb.gmm_bf16_fwd(h, wo_bf, gsd, False)
+    rel = ((yb.float() - y.float()).norm() / yb.float().norm()).item()
+    assert rel < 0.1, rel
+    del wo_c, wo_bf, y, yb
     # dLHS, contraction N = 3072: the default (CTA-pair) path against the oracle
     # on sampled rows and bit for bit against the streaming path
     dgu = W.cotangent(M, 2 * F, 23, device=DEV)

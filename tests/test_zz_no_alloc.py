@@ -75,3 +75,40 @@ def test_noalloc_rejects_sizes_past_its_scratch():
     rc = L.fp8moe_gmm_silu_fp8_fwd_noalloc(P(256), M, K, P(256), P(256), E, N, P(256), P(256),
                                            stream)
     assert rc == -3   # FP8MOE_EWORKSPACE, nothing launched
+
+
+def test_noalloc_at_exactly_the_scratch_size_through_the_binding():
+    """A problem whose workspace is exactly the 32 MiB array (the activation
+    codes and the row scales end at its last byte), through the Python binding:
+    the same bits as the regular entry point."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, K, N, E = 16352, 2048, 256, 4
+    assert fb.workspace_size(fb.OP_GMM_SILU_FP8_FWD, M, K, N, E) == fb.NOALLOC_SCRATCH_BYTES
+    x, codes, scale, gs = _case(M, K, N, E, [4000, 5000, 0, 7352], seed=31)
+    ref = fb.gmm_silu_fp8_fwd(x, codes, scale, gs)
+    out = torch.empty(M, N // 2, dtype=torch.bfloat16, device="cuda")
+    fb.gmm_silu_fp8_fwd_noalloc(x, codes, scale, gs, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert fb.read_status() == 0
+
+
+def test_noalloc_checks_arguments_before_the_size():
+    """A bad argument gets the regular entry point's code even when the size
+    would not fit either (nothing is launched in any of these calls)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    L = fb.load()
+    M, K, N, E = 8192, 7168, 256, 2
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    P = ctypes.c_void_p
+    # lhs not 16-byte aligned: FP8MOE_EALIGN
+    assert L.fp8moe_gmm_silu_fp8_fwd_noalloc(P(258), M, K, P(256), P(256), E, N, P(256), P(256),
+                                             stream) == -2
+    # null output: FP8MOE_EINVAL
+    assert L.fp8moe_gmm_silu_fp8_fwd_noalloc(P(256), M, K, P(256), P(256), E, N, P(256), None,
+                                             stream) == -1
+    # N not a multiple of 32 for SwiGLU: FP8MOE_EALIGN
+    assert L.fp8moe_gmm_silu_fp8_fwd_noalloc(P(256), M, K, P(256), P(256), E, 272, P(256),
+                                             P(256), stream) == -2
