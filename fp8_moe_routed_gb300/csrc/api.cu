@@ -124,24 +124,20 @@ struct TgmmWorkspace {
   float* sd;
 };
 
-// The code slots are kept in 128-column chunks, [S][ceil(C / 128)][128 rows][128]:
-// the tgmm then loads a segment's 256-column dout tile as one box.
 size_t tgmm_ws_bytes(int64_t M, int64_t K, int64_t N, int32_t E) {
   const size_t S = (size_t)segment_bound(M, E);
-  const size_t Kc = round_up((size_t)K, 128), Nc = round_up((size_t)N, 128);
-  return round_up(S * 128 * Kc, 256) + round_up(S * 128 * Nc, 256) +
+  return round_up(S * 128 * (size_t)K, 256) + round_up(S * 128 * (size_t)N, 256) +
          round_up(S * (size_t)K * 4, 256) + round_up(S * (size_t)N * 4, 256);
 }
 
 TgmmWorkspace carve_tgmm(void* ws, int64_t M, int64_t K, int64_t N, int32_t E) {
   const size_t S = (size_t)segment_bound(M, E);
-  const size_t Kc = round_up((size_t)K, 128), Nc = round_up((size_t)N, 128);
   uint8_t* p = static_cast<uint8_t*>(ws);
   TgmmWorkspace w;
   w.qx = p;
-  p += round_up(S * 128 * Kc, 256);
+  p += round_up(S * 128 * (size_t)K, 256);
   w.qd = p;
-  p += round_up(S * 128 * Nc, 256);
+  p += round_up(S * 128 * (size_t)N, 256);
   w.sx = reinterpret_cast<float*>(p);
   p += round_up(S * (size_t)K * 4, 256);
   w.sd = reinterpret_cast<float*>(p);
@@ -256,10 +252,10 @@ int dlhs_impl(const void* dout, int64_t M, int64_t N, const uint8_t* codes, cons
 
 int tgmm_quantize_impl(const void* lhs, const void* dout, int64_t M, int64_t K, int64_t N,
                        int32_t E, const int32_t* gs, uint8_t* qx, float* sx, uint8_t* qd,
-                       float* sd, cudaStream_t stream, int sms, int d_fmt, int chunked) {
+                       float* sd, cudaStream_t stream, int sms, int d_fmt) {
   cudaError_t e = fp8moe_launch_tgmm_quantize_tiles(lhs, dout, M, (int)K, (int)N, gs, E,
                                                     segment_bound(M, E), qx, sx, qd, sd, sms, 1,
-                                                    d_fmt, chunked, stream);
+                                                    d_fmt, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;
 }
@@ -362,25 +358,23 @@ static int tgmm_drhs_impl(const void* lhs, const void* dout, int64_t M, int64_t 
   const int64_t S = segment_bound(M, E);
   if (M > 0) {
     rc = tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, w.qx, w.sx, w.qd, w.sd, stream, sms,
-                            d_fmt, 1);
+                            d_fmt);
     if (rc) return rc;
   }
   TgmmArgs a;
   {
-    // chunked slots: [S * ceil(K / 128)][128 rows][128 columns], one chunk a box
-    const uint64_t dims[3] = {128, 128, (uint64_t)(S * ((K + 127) / 128))};
-    const uint64_t st[2] = {128, 128 * 128};
-    const uint32_t box[3] = {128, 128, 1};
-    rc = make_tmap(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.qx, dims, st, box,
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)(S * 128)};
+    const uint64_t st[1] = {(uint64_t)K};
+    const uint32_t box[2] = {128, 128};
+    rc = make_tmap(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w.qx, dims, st, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   {
-    // [S * ceil(N / 128)][128][128], two chunks (a 256-column tile) a box
-    const uint64_t dims[3] = {128, 128, (uint64_t)(S * ((N + 127) / 128))};
-    const uint64_t st[2] = {128, 128 * 128};
-    const uint32_t box[3] = {128, 128, 2};
-    rc = make_tmap(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.qd, dims, st, box,
+    const uint64_t dims[2] = {(uint64_t)N, (uint64_t)(S * 128)};
+    const uint64_t st[1] = {(uint64_t)N};
+    const uint32_t box[2] = {128, 128};
+    rc = make_tmap(&a.tmD, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w.qd, dims, st, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
@@ -601,9 +595,8 @@ int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M,
   int sms = 0;
   rc = device_init(&sms);
   if (rc) return rc;
-  // the parity export writes the row-major slot layout ([S][128][K], [S][128][N])
   return tgmm_quantize_impl(lhs, dout, M, K, N, E, group_sizes, qx, sx, qd, sd, stream, sms,
-                            dout_fmt, 0);
+                            dout_fmt);
 }
 
 int fp8moe_selftest_wait_timeout(uint32_t limit_us, fp8moe_stream_t stream) {

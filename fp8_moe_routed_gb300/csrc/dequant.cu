@@ -19,15 +19,17 @@ namespace fp8moe {
 constexpr int kDqThreads = 256;
 constexpr int kRows = 4;
 
-__device__ __forceinline__ void dequant16(uint4 c, const float* __restrict__ srow, int64_t n0,
-                                          uint32_t (&o)[8]) {
+__device__ __forceinline__ void load_scales16(const float* __restrict__ srow, int64_t n0,
+                                              float (&sc)[16]) {
   const float4* sp = reinterpret_cast<const float4*>(srow + n0);
-  float sc[16];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float4 f = __ldg(sp + i);
     sc[4 * i] = f.x; sc[4 * i + 1] = f.y; sc[4 * i + 2] = f.z; sc[4 * i + 3] = f.w;
   }
+}
+
+__device__ __forceinline__ void dequant16(uint4 c, const float (&sc)[16], uint32_t (&o)[8]) {
   const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -50,25 +52,38 @@ __device__ __forceinline__ void store32(uint4* dst, const uint32_t (&o)[8], bool
   }
 }
 
-__global__ void __launch_bounds__(kDqThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
-                                                                const float* __restrict__ scale,
-                                                                int64_t rows, int64_t K, int64_t N,
-                                                                uint4* __restrict__ out) {
+template <bool ONE_V>
+__global__ void __launch_bounds__(kDqThreads, 3) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                                   const float* __restrict__ scale,
+                                                                   int64_t rows, int64_t K, int64_t N,
+                                                                   uint4* __restrict__ out) {
   const int64_t vpr = N >> 4;   // 16-code vectors per row (N % 16 == 0)
   const bool v32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  // The kRows rows of a step share one expert (K % 16 == 0 and the first row is
+  // a multiple of kRows), so their scales are loaded once per step; when every
+  // thread owns a single vector of columns (ONE_V: N <= 16 * kDqThreads) they
+  // stay in registers until the expert changes. The load/store pipe, not DRAM,
+  // was the limit while every row reloaded them.
+  float sc[16];
+  int64_t e_keep = -1;
   // kRows rows per CTA step: every thread has kRows loads in flight
   for (int64_t r0 = (int64_t)blockIdx.x * kRows; r0 < rows; r0 += (int64_t)gridDim.x * kRows) {
+    const int64_t e = r0 / K;
     for (int64_t v = threadIdx.x; v < vpr; v += kDqThreads) {
       uint4 c[kRows];
 #pragma unroll
       for (int i = 0; i < kRows; ++i)
         c[i] = r0 + i < rows ? __ldg(reinterpret_cast<const uint4*>(codes + (r0 + i) * N) + v)
                              : make_uint4(0u, 0u, 0u, 0u);
+      if (!ONE_V || e != e_keep) {
+        load_scales16(scale + e * N, v << 4, sc);
+        e_keep = e;
+      }
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
         if (r0 + i < rows) {
           uint32_t o[8];
-          dequant16(c[i], scale + ((r0 + i) / K) * N, v << 4, o);
+          dequant16(c[i], sc, o);
           store32(out + (r0 + i) * (N >> 3) + 2 * v, o, v32);
         }
       }
@@ -84,10 +99,14 @@ cudaError_t fp8moe_launch_dequantize(const uint8_t* codes, const float* scale, i
                                      int64_t N, void* out, int num_sms, cudaStream_t s) {
   const int64_t rows = (int64_t)E * K;
   const int64_t blocks = (rows + fp8moe::kRows - 1) / fp8moe::kRows;
-  const int64_t cap = (int64_t)num_sms * 8;   // 8 CTAs of 256 threads per SM
+  const int64_t cap = (int64_t)num_sms * 3;   // the 3 CTAs of 256 threads resident per SM
   int grid = (int)(blocks < cap ? blocks : cap);
   if (grid < 1) grid = 1;
-  fp8moe::dequantize_kernel<<<grid, fp8moe::kDqThreads, 0, s>>>(codes, scale, rows, K, N,
-                                                                static_cast<uint4*>(out));
+  if (N <= 16 * fp8moe::kDqThreads)
+    fp8moe::dequantize_kernel<true><<<grid, fp8moe::kDqThreads, 0, s>>>(
+        codes, scale, rows, K, N, static_cast<uint4*>(out));
+  else
+    fp8moe::dequantize_kernel<false><<<grid, fp8moe::kDqThreads, 0, s>>>(
+        codes, scale, rows, K, N, static_cast<uint4*>(out));
   return cudaGetLastError();
 }

@@ -17,7 +17,7 @@ cudaError_t fp8moe_launch_quantize_rows_block(const void* lhs, int64_t M, int K,
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
-                                              int num_sms, int report, int d_fmt, int chunked,
+                                              int num_sms, int report, int d_fmt,
                                               cudaStream_t s);
 cudaError_t fp8moe_launch_dequantize(const uint8_t* codes, const float* scale, int E, int64_t K,
                                      int64_t N, void* out, int num_sms, cudaStream_t s);

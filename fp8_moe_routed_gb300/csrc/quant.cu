@@ -340,11 +340,10 @@ __device__ __forceinline__ void build_segments_warp0(const int32_t* s_begin, con
 // The segment's rows of the chunk are staged once in shared memory by cp.async
 // (one HBM read, no staging registers), the per-column amax comes from there,
 // then every thread casts its own 16-byte pieces into the zero-padded slot.
-// Two staging buffers: the CTA's next unit loads while this one is reduced and
-// cast, so each CTA keeps a tile in flight through its compute phases. Shared
-// memory is the two tiles plus per-expert bounds sized by E.
+// Shared memory is the staged tile plus per-expert bounds sized by E, so that
+// several CTAs per SM keep loads in flight while others compute.
 constexpr int kTQThreads = 256;
-constexpr int kTQMinBlocks = 3;            // CTAs per SM the register budget allows
+constexpr int kTQMinBlocks = 4;            // CTAs per SM the register budget allows
 constexpr int kTQCols = 128;
 constexpr int kTQRowBytes = kTQCols * 2;   // 256 B of bf16 per staged row
 constexpr size_t kTQTileBytes = 128 * (size_t)kTQRowBytes;      // 32 KB
@@ -353,43 +352,20 @@ constexpr int kTQRowStep = kTQThreads / kTQPieces;              // rows between 
 constexpr int kTQRowsPer = 128 / kTQRowStep;                    // rows per thread
 constexpr size_t kTQPartBytes = (kTQThreads / 32) * kTQPieces * 16;   // per warp and piece: 4 bf16x2 amax
 static_assert(kTQPieces <= 32 && kTQRowsPer * kTQRowStep == 128, "tile geometry");
-// dynamic shared memory: [tile x 2][part][scale][rl][rh][begin E][end E][segbase E + 1]
+// dynamic shared memory: [tile][part][scale][rl][rh][begin E][end E][segbase E + 1]
 __host__ __device__ constexpr size_t tq_smem_bytes(int E) {
-  return 2 * kTQTileBytes + kTQPartBytes + 3 * kTQCols * 4 + (size_t)(3 * E + 1) * 4;
-}
-
-// The rows [lo, hi) of slot t * 128 .. of one 128-column chunk of lhs or dout.
-struct TQUnit {
-  int qi, e, t, lo, hi, C, c0, ncols;
-  bool is_x;
-};
-
-__device__ __forceinline__ TQUnit tq_unit(int64_t u, bool small, int cpq, int ck, int K, int N,
-                                          const int32_t* s_begin, const int32_t* s_end,
-                                          const int32_t* s_segbase, int E) {
-  TQUnit r;
-  r.qi = small ? (int)((uint32_t)u / (uint32_t)cpq) : (int)(u / cpq);
-  const int ch = (int)(u - (int64_t)r.qi * cpq);
-  r.e = find_bucket(s_segbase, E, r.qi);
-  r.t = s_begin[r.e] / 128 + (r.qi - s_segbase[r.e]);
-  const int r0 = max(s_begin[r.e], r.t * 128), r1 = min(s_end[r.e], r.t * 128 + 128);
-  r.lo = r0 - r.t * 128;
-  r.hi = r1 - r.t * 128;
-  r.is_x = ch < ck;
-  r.C = r.is_x ? K : N;
-  r.c0 = (r.is_x ? ch : ch - ck) * kTQCols;
-  r.ncols = min(kTQCols, r.C - r.c0);                          // multiple of 16
-  return r;
+  return kTQTileBytes + kTQPartBytes + 3 * kTQCols * 4 + (size_t)(3 * E + 1) * 4;
 }
 
 __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_kernel(
     const __nv_bfloat16* __restrict__ lhs, const __nv_bfloat16* __restrict__ dout, int64_t M,
     int K, int N, const int32_t* __restrict__ gs, int E, int64_t Smax,
     uint8_t* __restrict__ qx, float* __restrict__ sx, uint8_t* __restrict__ qd,
-    float* __restrict__ sd, int report, int d_fmt, int chunked) {
+    float* __restrict__ sd, int report, int d_fmt) {
   extern __shared__ __align__(16) uint8_t tq_smem[];
-  uint4* s_part = reinterpret_cast<uint4*>(tq_smem + 2 * kTQTileBytes);   // [warp][piece]
-  float* s_scale = reinterpret_cast<float*>(tq_smem + 2 * kTQTileBytes + kTQPartBytes);
+  uint8_t* s_tile = tq_smem;                                     // [row][128 bf16]
+  uint4* s_part = reinterpret_cast<uint4*>(tq_smem + kTQTileBytes);   // [warp][piece]
+  float* s_scale = reinterpret_cast<float*>(tq_smem + kTQTileBytes + kTQPartBytes);
   float* s_rl = s_scale + kTQCols;                               // quotient brackets per column
   float* s_rh = s_rl + kTQCols;
   int32_t* s_begin = reinterpret_cast<int32_t*>(s_rh + kTQCols);
@@ -412,45 +388,34 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
   const int prow = tid / kTQPieces;   // first row of this thread, step kTQRowStep
   const int warp = tid >> 5, lane = tid & 31;
   const bool small = units < (int64_t(1) << 31);   // 32-bit unit arithmetic
-  // stage: rows [lo, hi) of the unit's slot, 16 threads per 256-byte row, as
-  // one cp.async group of this thread
-  auto stage = [&](int64_t uu, uint8_t* tile) {
-    const TQUnit w = tq_unit(uu, small, cpq, ck, K, N, s_begin, s_end, s_segbase, E);
-    if (piece * 8 < w.ncols) {
-      const __nv_bfloat16* src = w.is_x ? lhs : dout;
-      const __nv_bfloat16* sp = src + (int64_t)(w.t * 128 + prow) * w.C + w.c0 + piece * 8;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int qi = small ? (int)((uint32_t)u / (uint32_t)cpq) : (int)(u / cpq);
+    const int ch = (int)(u - (int64_t)qi * cpq);
+    const int e = find_bucket(s_segbase, E, qi);
+    const int t = s_begin[e] / 128 + (qi - s_segbase[e]);
+    const int r0 = max(s_begin[e], t * 128), r1 = min(s_end[e], t * 128 + 128);
+    const int lo = r0 - t * 128, hi = r1 - t * 128;            // slot rows of the segment
+    const bool is_x = ch < ck;
+    const bool e5 = !is_x && d_fmt == 1;                        // e5m2 codes
+    const float fmax = e5 ? kE5m2Max : kE4m3Max;
+    const int C = is_x ? K : N;
+    const int c0 = (is_x ? ch : ch - ck) * kTQCols;
+    const int ncols = min(kTQCols, C - c0);                     // multiple of 16
+    const __nv_bfloat16* src = is_x ? lhs : dout;
+    uint8_t* qo = (is_x ? qx : qd) + (int64_t)qi * 128 * C + c0 + piece * 8;
+    float* so = (is_x ? sx : sd) + (int64_t)qi * C;
+    const bool pin = piece * 8 < ncols;
+    // stage: rows [lo, hi) of the slot, 16 threads per 256-byte row
+    if (pin) {
+      const __nv_bfloat16* sp = src + (int64_t)(t * 128 + prow) * C + c0 + piece * 8;
 #pragma unroll
       for (int i = 0; i < kTQRowsPer; ++i) {
         const int rr = prow + kTQRowStep * i;
-        if (rr >= w.lo && rr < w.hi)
-          cp_async16(tile + rr * kTQRowBytes + piece * 16, sp + (int64_t)kTQRowStep * i * w.C, 16u);
+        if (rr >= lo && rr < hi)
+          cp_async16(s_tile + rr * kTQRowBytes + piece * 16, sp + (int64_t)kTQRowStep * i * C, 16u);
       }
     }
-    cp_async_commit();
-  };
-  if ((int64_t)blockIdx.x < units) stage(blockIdx.x, tq_smem);
-  int buf = 0;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x, buf ^= 1) {
-    const TQUnit w = tq_unit(u, small, cpq, ck, K, N, s_begin, s_end, s_segbase, E);
-    const int qi = w.qi, lo = w.lo, hi = w.hi, C = w.C, c0 = w.c0, ncols = w.ncols;
-    const bool is_x = w.is_x;
-    const bool e5 = !is_x && d_fmt == 1;                        // e5m2 codes
-    const float fmax = e5 ? kE5m2Max : kE4m3Max;
-    uint8_t* s_tile = tq_smem + buf * kTQTileBytes;
-    // the next unit's rows go to the other buffer while this one is worked on
-    // (that buffer's last reads ended at the previous unit's closing barrier)
-    if (u + gridDim.x < units) stage(u + gridDim.x, tq_smem + (buf ^ 1) * kTQTileBytes);
-    else cp_async_commit();                                     // an empty group
-    // slot layout: row-major [S][128][C] (row stride C), or chunked
-    // [S][ceil(C / 128)][128][128] (row stride 128: the unit's 128 columns form
-    // one contiguous 16 KB block, and a run of chunks is one tensor-map box)
-    const int64_t rstride = chunked ? kTQCols : C;
-    uint8_t* qo = (is_x ? qx : qd) + piece * 8 +
-                  (chunked ? ((int64_t)qi * ((C + kTQCols - 1) / kTQCols) + c0 / kTQCols) * 128 * kTQCols
-                           : (int64_t)qi * 128 * C + c0);
-    float* so = (is_x ? sx : sd) + (int64_t)qi * C;
-    const bool pin = piece * 8 < ncols;
-    cp_async_wait_group<1>();            // this unit's group has landed
+    cp_async_wait_all();
     __syncthreads();
     // column amax over the segment rows (exact): each thread reduces the rows
     // of its 16-byte piece that it casts later, the row sets of a warp meet by
@@ -497,9 +462,8 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
       }
     }
     __syncthreads();
-    // cast: every slot row is written, rows outside the segment as zeros (and in
-    // the chunked layout the columns past C of the last chunk as zeros too)
-    if (pin || chunked) {
+    // cast: every slot row is written, rows outside the segment as zeros
+    if (pin) {
       float sc[8], rl[8], rh[8];
 #pragma unroll
       for (int j = 0; j < 8; j += 4) {
@@ -514,7 +478,7 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
       for (int i = 0; i < kTQRowsPer; ++i) {
         const int rr = prow + kTQRowStep * i;
         uint2 o = make_uint2(0u, 0u);
-        if (pin && rr >= lo && rr < hi) {
+        if (rr >= lo && rr < hi) {
           const uint4 x = *reinterpret_cast<const uint4*>(s_tile + rr * kTQRowBytes + piece * 16);
           const uint32_t w[4] = {x.x, x.y, x.z, x.w};
           uint16_t c[4];
@@ -534,7 +498,7 @@ __global__ void __launch_bounds__(kTQThreads, kTQMinBlocks) tgmm_quantize_tiles_
           o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
           o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
         }
-        *reinterpret_cast<uint2*>(qo + (int64_t)rr * rstride) = o;
+        *reinterpret_cast<uint2*>(qo + (int64_t)rr * C) = o;
       }
     }
     __syncthreads();   // the tile and scales are reused by the next unit
@@ -604,21 +568,17 @@ cudaError_t fp8moe_launch_quantize_rows_block(const void* lhs, int64_t M, int K,
 cudaError_t fp8moe_launch_tgmm_quantize_tiles(const void* lhs, const void* dout, int64_t M, int K,
                                               int N, const int32_t* gs, int E, int64_t Smax,
                                               uint8_t* qx, float* sx, uint8_t* qd, float* sd,
-                                              int num_sms, int report, int d_fmt, int chunked,
-                                              cudaStream_t s) {
+                                              int num_sms, int report, int d_fmt, cudaStream_t s) {
   using namespace fp8moe;
-  const size_t smem = tq_smem_bytes(E);   // two 32 KB tiles + bounds: < 80 KB for E <= kMaxExperts
-  cudaError_t err = cudaFuncSetAttribute(tgmm_quantize_tiles_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  const size_t smem = tq_smem_bytes(E);   // < 48 KB for any E <= kMaxExperts
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tgmm_quantize_tiles_kernel,
-                                                      kTQThreads, smem);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, tgmm_quantize_tiles_kernel, kTQThreads, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int grid = num_sms * per_sm;   // one resident wave, grid-stride over units
   tgmm_quantize_tiles_kernel<<<grid, kTQThreads, smem, s>>>(
       static_cast<const __nv_bfloat16*>(lhs), static_cast<const __nv_bfloat16*>(dout), M, K, N,
-      gs, E, Smax, qx, sx, qd, sd, report, d_fmt, chunked);
+      gs, E, Smax, qx, sx, qd, sd, report, d_fmt);
   return cudaGetLastError();
 }

@@ -16,10 +16,8 @@
 // 256-wide n tile); n tiles of one k tile are adjacent so the A slots are
 // shared through L2.
 //   warp 0      lane 0: TMA of the qx slot [128 rows x 128 k] and the qd slot
-//               [128 rows x 256 n], MN-major operands, 128-byte swizzle. The
-//               slots are stored in 128-column chunks ([segment][chunk][row]
-//               [128]), so the qd tile's two chunks are one 32 KB box: two
-//               TMA operations per segment. All 32 lanes: the
+//               [128 rows x 256 n] (two 128-column boxes), row-major =
+//               MN-major operands, 128-byte swizzle. All 32 lanes: the
 //               segment's 128 + 256 channel scales by 16-byte cp.async into a
 //               scale ring (load/store unit, so the TMA unit only moves tiles).
 //   warp 1      tcgen05.mma kind::f8f6f4, M=128 (k), N=256 (n), K=32 rows, four
@@ -122,7 +120,6 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
   Smem& s = *reinterpret_cast<Smem*>(tiles + (size_t)kStages * kStageBytes + kEpiWarps * kXpose);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkt = (K + kBK - 1) / kBK, nnt = (N + kBN - 1) / kBN;
-  const int nnc = (N + 127) / 128;                // 128-column qd chunks per segment
   const int units_per_e = nkt * nnt;
 
   if (warp == 0) {
@@ -208,12 +205,9 @@ tgmm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUt
         if (lane == 0) {
           mbar_arrive_expect_tx(&s.full[st], kStageBytes);
           uint8_t* a = tiles + st * kStageBytes;
-          // chunked slots: the qx chunk kt of segment q, and qd chunks 2 ntile and
-          // 2 ntile + 1 in one box (past the last chunk of a segment that box
-          // reads the next segment's first chunk, or zeros at the very end:
-          // those columns are past N and never stored)
-          tma_load_3d(a, &tmX, &s.full[st], 0, 0, q * nkt + kt);
-          tma_load_3d(a + kXBytes, &tmD, &s.full[st], 0, 0, q * nnc + 2 * ntile);
+          tma_load_2d(a, &tmX, &s.full[st], kt * kBK, q * 128);
+          tma_load_2d(a + kXBytes, &tmD, &s.full[st], ntile * kBN, q * 128);
+          tma_load_2d(a + kXBytes + kDChunk, &tmD, &s.full[st], ntile * kBN + 128, q * 128);
         }
         const float* sxq = sx + (int64_t)q * K;
         const float* sdq = sd + (int64_t)q * N;
