@@ -1,0 +1,75 @@
+// quantize.cuh -- the activation quantization arithmetic shared by the
+// quantizer kernels (quant.cu) and the forward GMM's in-kernel row quantizer
+// (gmm_fwd.cu): scale = max(amax, 1e-12) / fmt_max by IEEE division, codes of
+// the correctly rounded f32 quotient x / scale ("MoE: native FP8 QAT for
+// routed-expert GMMs", Implementation: per-row full-K f32 scale).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace fp8moe {
+
+constexpr float kEps = 1e-12f;
+constexpr float kE4m3Max = 448.0f;
+constexpr float kE5m2Max = 57344.0f;
+
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t acc, uint32_t v) {
+  uint32_t a = v & 0x7FFF7FFFu, r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ float bf16x2_hmax_to_f32(uint32_t v) {
+  return fmaxf(bf16lo_to_f32(v), bf16hi_to_f32(v));
+}
+
+// Codes of the correctly rounded f32 quotients RN(x0 / s), RN(x1 / s), two per
+// conversion, from rl = RN(r * (1 - 2^-20)) and rh = RN(r * (1 + 2^-20)),
+// r = RN(1 / s).
+//   r is within 2^-24 of 1 / s (relative), rl and rh add 2^-24 each, and the
+//   products another 2^-24: x * rl and x * rh (as computed) lie more than 2^-21
+//   below and above x / s, and RN(x / s) within 2^-24 of it, so RN(x / s) is
+//   always between the two ends. Rounding to the fp8 grid (nearest, saturating)
+//   is monotonic: when both ends give the same code, every value between them
+//   does, RN(x / s) included. Otherwise a rounding boundary lies within ~2^-20
+//   of x / s (rare) and the exact IEEE quotients are converted instead. Below
+//   the f32 normal range the relative bounds fail, but such quotients and both
+//   ends then round to the zero code anyway. NaN and infinite x give the codes
+//   the quotient would (NaN; saturation).
+template <bool E5M2>
+__device__ __forceinline__ uint16_t cvt_x2(float a, float b) {
+  return E5M2 ? f32x2_to_e5m2x2(a, b) : f32x2_to_e4m3x2(a, b);
+}
+
+template <bool E5M2>
+__device__ __forceinline__ uint16_t quotient_x2(float x0, float x1, float s0, float s1, float rl0,
+                                                float rl1, float rh0, float rh1) {
+  const uint16_t lo = cvt_x2<E5M2>(__fmul_rn(x0, rl0), __fmul_rn(x1, rl1));
+  const uint16_t hi = cvt_x2<E5M2>(__fmul_rn(x0, rh0), __fmul_rn(x1, rh1));
+  if (lo == hi) return lo;
+  return cvt_x2<E5M2>(__fdiv_rn(x0, s0), __fdiv_rn(x1, s1));
+}
+
+__device__ __forceinline__ void bracket(float s, float& rl, float& rh) {
+  const float r = __frcp_rn(s);
+  rl = __fmul_rn(r, 1.0f - 0x1p-20f);
+  rh = __fmul_rn(r, 1.0f + 0x1p-20f);
+}
+
+// 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2).
+__device__ __forceinline__ uint2 quant8(uint4 v, float s, float rl, float rh) {
+  uint2 o;
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint16_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = quotient_x2<false>(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), s, s, rl, rl, rh, rh);
+  o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+  o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+  return o;
+}
+
+}  // namespace fp8moe

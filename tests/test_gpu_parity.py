@@ -108,6 +108,39 @@ def test_gmm_fwd_vs_oracle(orc, M, K, N, E, gs, silu):
     assert (out[T:].float() == 7.0).all(), "rows >= T were written"
 
 
+@pytest.mark.parametrize("silu", [True, False])
+@pytest.mark.parametrize("M,K,N,gs", [
+    (512, 256, 256, "tiny"), (700, 512, 512, [300, 0, 129, 1, 200]),
+    (200, 7168, 256, [64, 64, 0, 60]), (64, 9216, 64, [40, 24]), (130, 64, 64, [129, 1]),
+    (2048, 2048, 256, [1000, 0, 1000, 47]),
+])
+def test_gmm_fwd_inkernel_codes_and_scales_bit_exact(orc, M, K, N, gs, silu):
+    """The forward quantizes its activation rows inside the GMM kernel into the
+    workspace (codes [M, K], then the row scales [M]): after the call those are
+    bit-exact against the oracle's quantization for every row < T, and the
+    output is still within tolerance."""
+    gs = W.group_sizes("tiny", seed=2, M=M) if gs == "tiny" else torch.tensor(gs, dtype=torch.int32)
+    E = gs.numel()
+    T = int(gs.sum())
+    x = W.fill_tail_garbage(W.activations(M, K, seed=K + M, outlier_frac=0.05), T)
+    x[0, :] = 0
+    codes, scale = W.fp8_weights(E, K, N, 0.02, seed=7)
+    op = fb.OP_GMM_SILU_FP8_FWD if silu else fb.OP_GMM_FP8_FWD
+    ws = torch.zeros(fb.workspace_size(op, M, K, N, E), dtype=torch.uint8, device=DEV)
+    fn = fb.gmm_silu_fp8_fwd if silu else fb.gmm_fp8_fwd
+    out = fn(*cuda(x, codes, scale, gs), workspace=ws)
+    q = ws[:M * K].view(M, K).cpu()
+    off = (M * K + 255) // 256 * 256
+    sx = ws[off:off + 4 * M].view(torch.float32).cpu()
+    q_ref, sx_ref, bad = orc.quantize_rows(x, gs)
+    assert bad == 0
+    assert torch.equal(sx[:T], sx_ref[:T])
+    assert torch.equal(q[:T], q_ref[:T])
+    ref, _, bad = orc.gmm_fwd(x, codes, scale, gs, silu=silu)
+    assert bad == 0
+    check_bf16(out[:T], ref[:T], what="fwd with in-kernel quantization")
+
+
 def test_gmm_fwd_all_groups_empty():
     M, K, N, E = 256, 256, 256, 4
     x, codes, scale, gs = fwd_case(M, K, N, E, [0, 0, 0, 0], seed=3)

@@ -87,7 +87,9 @@ def _shard_worker(rank, world, port, q, sizes):
     mine = (sh.e0, sh.e1, sh.row0, sh.row1, h.view(torch.int16), dx.view(torch.int16), dw)
     got = [None] * world
     dist.all_gather_object(got, mine)
-    q.put((rank, got))
+    # plain numpy arrays through the queue: a tensor would travel as a shared-
+    # memory handle that can vanish when this process exits before it is read
+    q.put((rank, [tuple(x.numpy() if torch.is_tensor(x) else x for x in g) for g in got]))
     dist.destroy_process_group()
 
 
@@ -119,6 +121,8 @@ def test_expert_parallel_shards_reassemble_the_single_rank_result(sizes, aligned
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
+    res = {r: [tuple(torch.from_numpy(x) if hasattr(x, "dtype") else x for x in g) for g in v]
+           for r, v in res.items()}
     # both ranks gathered the same shards
     assert all(torch.equal(a, b) if torch.is_tensor(a) else a == b
                for s0, s1 in zip(res[0], res[1]) for a, b in zip(s0, s1))
