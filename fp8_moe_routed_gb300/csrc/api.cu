@@ -107,11 +107,8 @@ struct FwdWorkspace {
   float* sx;
 };
 
-// forward workspace: the activation codes [M, K], the row scales [M] and one
-// ready counter per 128-row block (the in-kernel quantizer publishes rows there)
 size_t fwd_ws_bytes(int64_t M, int64_t K) {
-  return round_up((size_t)M * (size_t)K, 256) + round_up((size_t)M * 4, 256) +
-         round_up((size_t)((M + 127) / 128) * 4, 256);
+  return round_up((size_t)M * (size_t)K, 256) + round_up((size_t)M * 4, 256);
 }
 
 constexpr int64_t kQuantBlock = 512;
@@ -166,7 +163,6 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   if (rc) return rc;
   uint8_t* q = static_cast<uint8_t*>(ws);
   float* sx = reinterpret_cast<float*>(q + round_up((size_t)M * (size_t)K, 256));
-  int* ready = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sx) + round_up((size_t)M * 4, 256));
   GmmFwdArgs a;
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
@@ -193,17 +189,12 @@ int gmm_fp8_fwd_impl(const void* lhs, int64_t M, int64_t K, const uint8_t* codes
   a.N = (int)N;
   a.E = E;
   a.swiglu = swiglu;
-  // the GMM quantizes the activation rows itself (four warps of every CTA),
-  // publishing each 128-row block on a counter that starts at zero
-  cudaError_t e = cudaMemsetAsync(ready, 0, (size_t)((M + 127) / 128) * 4, stream);
+  cudaError_t e = fp8moe_launch_quantize_rows(lhs, M, (int)K, gs, E, 0, E, q, sx, sms, 8, 1,
+                                              stream);
   if (e != cudaSuccess) return cuda_fail(e);
   a.e0 = 0;
   a.e1 = E;
   a.blk = 0;
-  a.fuseq = 1;
-  a.lhs = lhs;
-  a.q = q;
-  a.ready = ready;
   e = fp8moe_launch_gmm_fp8_fwd(a, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return FP8MOE_OK;

@@ -31,8 +31,8 @@
 //   warp 0       TMA: this CTA's dout half [128 rows x 64] bf16 (K-major,
 //                128-byte swizzle; completion counted on the even CTA's barrier)
 //                and its codes [128 k x 64 n] (64-byte swizzle), 8 stages; the
-//                step's 64 weight scales ride on the codes' barrier (cp.async
-//                by 16 lanes), so the dequant warps never wait on global loads.
+//                step's 64 weight scales ride on the codes' barrier (a bulk
+//                copy), so the dequant warps never wait on global loads.
 //   warp 1       TMEM (512 columns: accumulator [0, 256), eight 32-column A
 //                slots [256, 512)); in the even CTA the MMA-issuing thread.
 //   warps 2, 3   idle (they complete the first warpgroup for setmaxnreg).
@@ -69,7 +69,6 @@ constexpr int kBBytes = kRows * kBK * 2;      // 16 KB dout half
 constexpr int kCBytes = kRows * kBK;          // 8 KB codes
 constexpr int kStageBytes = kBBytes + kCBytes;
 constexpr int kScaleBytes = kBK * 4;          // a step's weight scales
-constexpr int kScaleLanes = kScaleBytes / 16; // producer lanes copying them, 16 bytes each
 constexpr int kASlots = 8;
 constexpr int kACols = kBK / 2;               // TMEM columns per A slot (bf16 pairs)
 constexpr int kDCols = kUnitRows;             // accumulator columns
@@ -198,7 +197,7 @@ gmm_dlhs_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     if (lane == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(&s.bfull[i], 1);
-        mbar_init(&s.cfull[i], 1 + kScaleLanes);   // the tile's expect_tx + the scale copies
+        mbar_init(&s.cfull[i], 1);
         mbar_init(&s.sempty[i], 1 + kDqWarps / 4);   // the MMA commit + one dequant group
       }
       for (int i = 0; i < kASlots; ++i) {
@@ -224,40 +223,29 @@ gmm_dlhs_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
   if (warp < kCtlWarps) setmaxnreg_dec<kCtlRegs>();
   if (warp == 0) {
     // ============================ TMA producer ============================
-    // lane 0 issues the two tensor copies of a step (dout half, codes); lanes
-    // 0..15 copy the step's 64 weight scales by 16-byte cp.async (load/store
-    // unit), each counting one arrival on the codes' barrier once its copy has
-    // landed, so the TMA unit moves only the two tiles
-    int st = 0;
-    uint32_t ph = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    for (int u = cluster; u < total && ok; u += nclusters) {
-      const Unit t = decode_unit(s, E, nkt, u);
-      for (int kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait_warp_cluster(&s.sempty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
-        if (lane == 0) {
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int u = cluster; u < total && ok; u += nclusters) {
+        const Unit t = decode_unit(s, E, nkt, u);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(&s.sempty[st], ph ^ 1, kWhereProducer)) { ok = false; break; }
           if (rank == 0) mbar_arrive_expect_tx(&s.bfull[st], 2 * kBBytes);
           tma_load_2d_pair(b_tile(st), &tmA, mapa_shared(smem_u32(&s.bfull[st]), 0), kb * kBK,
                            t.m0 + rank * kRows);
-          mbar_arrive_expect_tx(&s.cfull[st], kCBytes);
+          // N % 16 == 0: the in-range scales of a step are a multiple of 64 bytes
+          const uint32_t sbytes = (uint32_t)min(kBK, N - kb * kBK) * 4u;
+          mbar_arrive_expect_tx(&s.cfull[st], kCBytes + sbytes);
           tma_load_3d(c_tile(st), &tmC, &s.cfull[st], kb * kBK, t.k0 + rank * kRows, t.e);
+          bulk_load(scales + st * kBK, scale + (int64_t)t.e * N + kb * kBK, sbytes, &s.cfull[st]);
+          ++issued;
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
-        if (lane < kScaleLanes) {
-          // N % 16 == 0: a group of 4 scales is all in range or all past N (zeros)
-          const int c = kb * kBK + lane * 4;
-          const uint32_t b = c < N ? 16u : 0u;
-          cp_async16(scales + st * kBK + lane * 4, b ? scale + (int64_t)t.e * N + c : scale, b);
-          cp_async_mbar_arrive(&s.cfull[st]);
-        }
-        ++issued;
-        if (++st == kStages) { st = 0; ph ^= 1; }
       }
-    }
-    cp_async_wait_all();
-    // drain: every copy into this CTA (and, for the even CTA, both dout
-    // halves) landed before either CTA may exit
-    if (lane == 0) {
+      // drain: every copy into this CTA (and, for the even CTA, both dout
+      // halves) landed before either CTA may exit
       const int64_t n_last = issued < kStages ? issued : kStages;
       for (int64_t i = 1; i <= n_last; ++i) {
         const int64_t idx = issued - i;

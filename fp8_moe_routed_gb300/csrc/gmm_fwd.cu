@@ -42,7 +42,6 @@
 #include "ptx.cuh"
 #include "groups.cuh"
 #include "kernels.h"
-#include "quantize.cuh"
 
 namespace fp8moe {
 namespace fwd {
@@ -59,16 +58,12 @@ constexpr int kStageBytes = kABytes + kBBytes;
 // per SM sub-partition: 10 warps put 3 on two of them, so a thread may hold
 // 16384 / (3 * 32) -> 168 registers (launch bounds of 384 threads give the
 // compiler that cap); 6 warps put at most 2 on one, which leaves the cap at 255.
-// FUSEQ: four more warps quantize the activation rows inside the kernel (see
-// quantize_rows_inkernel); 14 warps put 4 on a sub-partition, a 128-register cap.
-template <bool SWIGLU, bool BLK, bool FUSEQ = false>
+template <bool SWIGLU, bool BLK>
 struct Epi {
   static constexpr int kWarps = (SWIGLU || BLK) ? 8 : 4;
   static constexpr int kHalves = kWarps / 4;
-  static constexpr int kQWarps = FUSEQ ? 4 : 0;
-  static constexpr int kThreads = (2 + kWarps + kQWarps) * 32;
-  static constexpr int kRegBudgetThreads =
-      (2 + kWarps + kQWarps) > 12 ? 512 : ((2 + kWarps + kQWarps) > 8 ? 384 : 192);
+  static constexpr int kThreads = (2 + kWarps) * 32;
+  static constexpr int kRegBudgetThreads = kWarps == 8 ? 384 : 192;
 };
 constexpr int kTmemCols = 512;
 
@@ -132,82 +127,14 @@ __device__ __forceinline__ void store_row_chunk(const uint32_t* o, bool row_ok,
   }
 }
 
-// In-kernel activation quantization (FUSEQ): the grid's nq quantizer warps take
-// the rows lo + w, lo + w + nq, ... below hi (w = this warp's index among them),
-// each row in two passes over its K values (the amax from HBM, then the cast of
-// the same 16-byte pieces, now in L2) with the arithmetic of quantize_rows_kernel
-// (same codes and scales, bit for bit). A row is published by counting it on the
-// ready counter of its 128-row block: every lane fences its stores first, so a
-// thread that reads the counter with acquire semantics sees the row's codes and
-// scale. The quantizer warps wait on nothing, so every counter reaches its
-// target once all CTAs of the grid are resident (one CTA per SM, grid = SMs).
-__device__ __forceinline__ void quantize_rows_inkernel(const __nv_bfloat16* __restrict__ lhs, int K,
-                                                       int64_t lo, int64_t hi, int64_t w, int64_t nq,
-                                                       uint8_t* q, float* sx, int* ready, int lane) {
-  const int nchunk = K >> 3;   // 16-byte pieces per row (K % 16 == 0)
-  for (int64_t m = lo + w; m < hi; m += nq) {
-    const uint4* row = reinterpret_cast<const uint4*>(lhs + m * K);
-    uint32_t a2 = 0;
-    int c = lane;
-    for (; c + 96 < nchunk; c += 128) {     // four loads in flight per lane
-      const uint4 v0 = __ldg(row + c), v1 = __ldg(row + c + 32), v2 = __ldg(row + c + 64),
-                  v3 = __ldg(row + c + 96);
-      a2 = bf16x2_absmax(a2, v0.x); a2 = bf16x2_absmax(a2, v0.y);
-      a2 = bf16x2_absmax(a2, v0.z); a2 = bf16x2_absmax(a2, v0.w);
-      a2 = bf16x2_absmax(a2, v1.x); a2 = bf16x2_absmax(a2, v1.y);
-      a2 = bf16x2_absmax(a2, v1.z); a2 = bf16x2_absmax(a2, v1.w);
-      a2 = bf16x2_absmax(a2, v2.x); a2 = bf16x2_absmax(a2, v2.y);
-      a2 = bf16x2_absmax(a2, v2.z); a2 = bf16x2_absmax(a2, v2.w);
-      a2 = bf16x2_absmax(a2, v3.x); a2 = bf16x2_absmax(a2, v3.y);
-      a2 = bf16x2_absmax(a2, v3.z); a2 = bf16x2_absmax(a2, v3.w);
-    }
-    for (; c < nchunk; c += 32) {
-      const uint4 v = __ldg(row + c);
-      a2 = bf16x2_absmax(a2, v.x); a2 = bf16x2_absmax(a2, v.y);
-      a2 = bf16x2_absmax(a2, v.z); a2 = bf16x2_absmax(a2, v.w);
-    }
-    float amax = bf16x2_hmax_to_f32(a2);
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    const float sc = __fdiv_rn(fmaxf(amax, kEps), kE4m3Max);
-    float rl, rh;
-    bracket(sc, rl, rh);
-    uint2* qrow = reinterpret_cast<uint2*>(q + m * K);
-    c = lane;
-    for (; c + 32 < nchunk; c += 64) {
-      const uint4 v0 = __ldg(row + c), v1 = __ldg(row + c + 32);
-      qrow[c] = quant8(v0, sc, rl, rh);
-      qrow[c + 32] = quant8(v1, sc, rl, rh);
-    }
-    for (; c < nchunk; c += 32) qrow[c] = quant8(__ldg(row + c), sc, rl, rh);
-    if (lane == 0) sx[m] = sc;
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence();   // cumulative: orders the whole warp's row before the count
-      atomicAdd(ready + (m >> 7), 1);
-    }
-  }
-}
-
-// Rows of block b (rows [128 b, 128 b + 128)) that the in-kernel quantizer covers,
-// those inside [lo, hi): the target of the block's ready counter.
-__device__ __forceinline__ int block_rows(int64_t b, int64_t lo, int64_t hi) {
-  const int64_t a = b * 128 > lo ? b * 128 : lo;
-  const int64_t z = b * 128 + 128 < hi ? b * 128 + 128 : hi;
-  return z > a ? (int)(z - a) : 0;
-}
-
 // FP8: a 128-byte swizzle row holds 128 K values of A (or 128 N values of B);
 // BF16: 64.
-template <bool FP8, bool SWIGLU, bool BLK, bool FUSEQ>
-__global__ void __launch_bounds__(Epi<SWIGLU, BLK, FUSEQ>::kRegBudgetThreads, 1)
+template <bool FP8, bool SWIGLU, bool BLK>
+__global__ void __launch_bounds__(Epi<SWIGLU, BLK>::kRegBudgetThreads, 1)
 gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               float* sx, const float* __restrict__ scale,
+               const float* __restrict__ sx, const float* __restrict__ scale,
                const int32_t* __restrict__ gs, __nv_bfloat16* __restrict__ out, int64_t M, int K,
-               int N, int E, int e0, int e1, const __nv_bfloat16* __restrict__ lhs, uint8_t* q,
-               int* ready) {
-  using EpiT = Epi<SWIGLU, BLK, FUSEQ>;
+               int N, int E, int e0, int e1) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -253,7 +180,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s.tfull[i], 1);
-        mbar_init(&s.tempty[i], 2 * EpiT::kWarps);   // one lane per epilogue warp, both CTAs
+        mbar_init(&s.tempty[i], 2 * Epi<SWIGLU, BLK>::kWarps);   // one lane per epilogue warp, both CTAs
       }
       mbar_init(&s.drain, 1);
       fence_mbar_init();
@@ -268,9 +195,6 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const int total = s.total_units;
   const uint32_t tmem = s.tmem_base;
-  // rows the in-kernel quantizer covers: those of experts [e0, e1)
-  const int64_t qlo = (FUSEQ && e0 < e1) ? s.begin[e0] : 0;
-  const int64_t qhi = (FUSEQ && e0 < e1) ? s.end[e1 - 1] : 0;
 
   if (warp == 0) {
     // ============================ TMA producer ============================
@@ -281,15 +205,6 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool ok = true;
       for (int u = cluster; u < total && ok; u += nclusters) {
         const Unit t = decode_unit(s, E, nt, u, rank);
-        if (FUSEQ && t.rows > 0) {
-          // this CTA's A rows are quantized (their blocks' counters reached
-          // their targets) before their codes are loaded by TMA
-          const int64_t b0 = t.row0 >> 7, b1 = (t.row0 + t.rows - 1) >> 7;
-          for (int64_t b = b0; b <= b1 && ok; ++b)
-            if (!wait_counter_geq(ready + b, block_rows(b, qlo, qhi), kWhereProducer)) ok = false;
-          if (!ok) break;
-          fence_proxy_async_global();
-        }
         int nb;
         if (SWIGLU) nb = (rank ? Nout : 0) + t.j * 128;
         else nb = t.j * kBN + rank * 128;
@@ -380,12 +295,12 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mma_commit_pair(&s.drain);
     }
     if (lane == 0) mbar_wait_cluster(&s.drain, 0, kWhereDrain);
-  } else if (warp < 2 + EpiT::kWarps) {
+  } else {
     // =============================== epilogue =============================
     const int et = threadIdx.x - 64;                 // epilogue thread
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter ..
-    constexpr int kEpiThreads = EpiT::kWarps * 32;
-    constexpr int kHalves = EpiT::kHalves;
+    constexpr int kEpiThreads = Epi<SWIGLU, BLK>::kWarps * 32;
+    constexpr int kHalves = Epi<SWIGLU, BLK>::kHalves;
     const int half = (warp - 2) >> 2;                // which half of the columns (8 warps)
     const int r = quarter * 32 + lane;               // row inside this CTA's tile
     int acc = 0;
@@ -494,19 +409,7 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         sb ^= 1;
         continue;
       }
-      float sxr = 1.0f;
-      if (FUSEQ) {
-        // the row's scale was written during this launch: acquire its block's
-        // counter (normally complete already: the producer waited on it), then
-        // read the scale through L2; a timeout fails the whole warp
-        bool okq = true;
-        if (row_ok && !failed)
-          okq = wait_counter_geq(ready + (row >> 7), block_rows(row >> 7, qlo, qhi), kWhereEpilogue);
-        if (!__all_sync(0xffffffffu, okq)) failed = true;
-        if (row_ok && !failed) sxr = __ldcg(sx + row);
-      } else if (FP8 && row_ok) {
-        sxr = __ldg(sx + row);
-      }
+      const float sxr = (FP8 && row_ok) ? __ldg(sx + row) : 1.0f;
       if (!failed && !mbar_wait_warp_cluster(&s.tfull[acc], aph, kWhereEpilogue)) failed = true;
       if (failed) {
         acc ^= 1;
@@ -572,11 +475,6 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (acc == 0) aph ^= 1;
       sb ^= 1;
     }
-  } else if (FUSEQ) {
-    // ========================== in-kernel quantizer ========================
-    const int qw = warp - 2 - EpiT::kWarps;
-    quantize_rows_inkernel(lhs, K, qlo, qhi, (int64_t)blockIdx.x * EpiT::kQWarps + qw,
-                           (int64_t)gridDim.x * EpiT::kQWarps, q, sx, ready, lane);
   }
 
   __syncthreads();
@@ -587,15 +485,15 @@ gmm_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <bool FP8, bool SWIGLU, bool BLK, bool FUSEQ>
+template <bool FP8, bool SWIGLU, bool BLK>
 cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
-  auto kern = gmm_fwd_kernel<FP8, SWIGLU, BLK, FUSEQ>;
+  auto kern = gmm_fwd_kernel<FP8, SWIGLU, BLK>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);   // whole CTA pairs, one CTA per SM
-  cfg.blockDim = dim3(Epi<SWIGLU, BLK, FUSEQ>::kThreads, 1, 1);
+  cfg.blockDim = dim3(Epi<SWIGLU, BLK>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -605,9 +503,8 @@ cudaError_t launch(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, const_cast<float*>(a.sx), a.scale, a.gs,
-                           static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N, a.E, a.e0, a.e1,
-                           static_cast<const __nv_bfloat16*>(a.lhs), a.q, a.ready);
+  err = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.sx, a.scale, a.gs,
+                           static_cast<__nv_bfloat16*>(a.out), a.M, a.K, a.N, a.E, a.e0, a.e1);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -620,17 +517,11 @@ FP8MOE_DEFINE_STATUS_TAKE(fp8moe_status_take_gmm_fwd)
 cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   using namespace fp8moe::fwd;
   if (a.blk)
-    return a.swiglu ? launch<true, true, true, false>(a, num_sms, s)
-                    : launch<true, false, true, false>(a, num_sms, s);
-  if (a.fuseq)
-    return a.swiglu ? launch<true, true, false, true>(a, num_sms, s)
-                    : launch<true, false, false, true>(a, num_sms, s);
-  return a.swiglu ? launch<true, true, false, false>(a, num_sms, s)
-                  : launch<true, false, false, false>(a, num_sms, s);
+    return a.swiglu ? launch<true, true, true>(a, num_sms, s) : launch<true, false, true>(a, num_sms, s);
+  return a.swiglu ? launch<true, true, false>(a, num_sms, s) : launch<true, false, false>(a, num_sms, s);
 }
 
 cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s) {
   using namespace fp8moe::fwd;
-  return a.swiglu ? launch<false, true, false, false>(a, num_sms, s)
-                  : launch<false, false, false, false>(a, num_sms, s);
+  return a.swiglu ? launch<false, true, false>(a, num_sms, s) : launch<false, false, false>(a, num_sms, s);
 }

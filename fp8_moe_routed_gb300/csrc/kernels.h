@@ -35,11 +35,6 @@ struct GmmFwdArgs {
   int e0, e1;             // only the units of experts [e0, e1)
   int blk;                // 1: sx holds per-512-column block scales [M, ceil(K/512)] and the
                           //    accumulation across blocks is bf16 (FP8 arm only)
-  int fuseq = 0;          // 1: the kernel quantizes lhs itself into the codes q (tmA's
-                          //    memory) and sx, publishing rows on ready (FP8 arm only)
-  const void* lhs = nullptr;   // bf16 [M, K] activations (fuseq)
-  uint8_t* q = nullptr;        // codes [M, K] (fuseq)
-  int* ready = nullptr;        // [ceil(M / 128)] row counters, zero at launch (fuseq)
 };
 cudaError_t fp8moe_launch_gmm_fp8_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);
 cudaError_t fp8moe_launch_gmm_bf16_fwd(const GmmFwdArgs& a, int num_sms, cudaStream_t s);

@@ -191,32 +191,6 @@ __device__ __forceinline__ void st_global_64B(void* p, const uint32_t* o) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Orders this thread's earlier generic-proxy accesses to global memory (here:
-// an acquire that observed another SM's published data) before its later
-// async-proxy ones (TMA reads of that data).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Bounded wait until *p >= target (a counter other SMs raise): false, with the
-// timeout recorded in the status word, after kWaitLimitNs.
-__device__ __forceinline__ bool wait_counter_geq(const int* p, int target, uint32_t where) {
-  if (ld_acquire_gpu(p) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (ld_acquire_gpu(p) >= target) return true;
-    if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
-      status_set(kStatusWaitTimeout | where);
-      return false;
-    }
-  }
-}
 
 // ------------------------------------------------------------------- tcgen05
 // Allocation is warp-wide; the TMEM base address is written to *dst_smem.

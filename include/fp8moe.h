@@ -89,14 +89,8 @@ size_t fp8moe_workspace_size(int op, int64_t M, int64_t K, int64_t N, int32_t E)
  *   qx     = e4m3(lhs[m,k] / sx[m])                       (RNE, saturating)
  *   out[m,n] = bf16( sx[m] * scale[e,n] * sum_k qx[m,k] * codes[e,k,n] )  (f32 accumulation)
  * lhs: bf16 [M, K].  codes: u8 [E, K, N].  scale: f32 [E, N].
- * out: bf16 [M, N]; rows >= T untouched.  Workspace: FP8MOE_OP_GMM_FP8_FWD,
- * laid out as the activation codes u8 [M, K] (256-byte padded), the row scales
- * f32 [M] (padded) and int32 counters [ceil(M/128)].  The quantization runs in
- * the GMM kernel: warps of every CTA quantize rows ahead of the tiles that read
- * them and count finished rows per 128-row block; the counters are zeroed on
- * `stream` first.  After the call the workspace holds the codes and scales of
- * rows < T.  The kernel relies on all of its CTAs being resident at once (one
- * per SM); a wait that outlasts its limit sets FP8MOE_STATUS_WAIT_TIMEOUT. */
+ * out: bf16 [M, N]; rows >= T untouched.  Workspace: FP8MOE_OP_GMM_FP8_FWD
+ * (holds the activation codes and row scales). */
 int fp8moe_gmm_fp8_fwd(const void* lhs, int64_t M, int64_t K, const uint8_t* codes,
                        const float* scale, int32_t E, int64_t N, const int32_t* group_sizes,
                        void* out, void* workspace, size_t workspace_bytes,

@@ -114,11 +114,11 @@ def test_gmm_fwd_vs_oracle(orc, M, K, N, E, gs, silu):
     (200, 7168, 256, [64, 64, 0, 60]), (64, 9216, 64, [40, 24]), (130, 64, 64, [129, 1]),
     (2048, 2048, 256, [1000, 0, 1000, 47]),
 ])
-def test_gmm_fwd_inkernel_codes_and_scales_bit_exact(orc, M, K, N, gs, silu):
-    """The forward quantizes its activation rows inside the GMM kernel into the
-    workspace (codes [M, K], then the row scales [M]): after the call those are
+def test_gmm_fwd_workspace_codes_and_scales_bit_exact(orc, M, K, N, gs, silu):
+    """The codes and row scales the forward GMM consumed are left in its
+    workspace (codes [M, K], then the row scales [M]): after the call they are
     bit-exact against the oracle's quantization for every row < T, and the
-    output is still within tolerance."""
+    output is within tolerance."""
     gs = W.group_sizes("tiny", seed=2, M=M) if gs == "tiny" else torch.tensor(gs, dtype=torch.int32)
     E = gs.numel()
     T = int(gs.sum())
