@@ -49,7 +49,7 @@ CSRC = os.path.join(ROOT, "fp8_moe_routed_gb300", "csrc")
 TRAFFIC = {
     # row quantizer + wi GMM (E=32 x 1024 rows, K=7168, N=4096)
     "wi_fwd": {"bytes": None, "sha1": None,
-               "sources": ("quant.cu", "gmm_fwd.cu", "ptx.cuh", "groups.cuh")},
+               "sources": ("quant.cu", "quantize.cuh", "gmm_fwd.cu", "ptx.cuh", "groups.cuh")},
     # the wi dLHS launch (contraction 4096, output 7168)
     "wi_dlhs": {"bytes": None, "sha1": None,
                 "sources": ("gmm_dlhs_pair.cu", "ptx.cuh", "groups.cuh")},

@@ -47,8 +47,13 @@ __device__ __forceinline__ uint16_t cvt_x2(float a, float b) {
 template <bool E5M2>
 __device__ __forceinline__ uint16_t quotient_x2(float x0, float x1, float s0, float s1, float rl0,
                                                 float rl1, float rh0, float rh1) {
-  const uint16_t lo = cvt_x2<E5M2>(__fmul_rn(x0, rl0), __fmul_rn(x1, rl1));
-  const uint16_t hi = cvt_x2<E5M2>(__fmul_rn(x0, rh0), __fmul_rn(x1, rh1));
+  // both bracket products as packed f32x2 multiplies (two RN multiplies each:
+  // the same bits as four scalar ones, in half the instructions)
+  float pl0, pl1, ph0, ph1;
+  mul_f32x2(x0, x1, rl0, rl1, pl0, pl1);
+  mul_f32x2(x0, x1, rh0, rh1, ph0, ph1);
+  const uint16_t lo = cvt_x2<E5M2>(pl0, pl1);
+  const uint16_t hi = cvt_x2<E5M2>(ph0, ph1);
   if (lo == hi) return lo;
   return cvt_x2<E5M2>(__fdiv_rn(x0, s0), __fdiv_rn(x1, s1));
 }
