@@ -643,7 +643,13 @@ def main():
     value = world * total_flops / (ms_step * 1e-3) / 1e12
 
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16"]            # fp8 dense = 2 x bf16 dense (nominal ratio)
+    # The step's kernels are timed inside a long loop: over half a second the
+    # part runs at its power-capped clock, so the denominator is the sustained
+    # (seconds-long) bf16 figure; a short region is compared with the burst one.
+    long_region = ms_total >= 500.0 and pk.get("bf16_sustained")
+    bf_peak = pk["bf16_sustained"] if long_region else pk["bf16"]
+    peak_kind = "sustained" if long_region else "burst"
+    fp8_peak = 2.0 * bf_peak               # fp8 dense = 2 x bf16 dense (nominal ratio)
     wi_tflops = flops["wi_fwd"] / (per["wi_fwd"] * 1e-3) / 1e12
     dl_tflops = flops["wi_dlhs"] / (per["wi_dlhs"] * 1e-3) / 1e12
     # algorithmic bytes per call: valid rows read once, weights read once,
@@ -658,8 +664,9 @@ def main():
     kern = {}
     for n in names:
         dl = "dlhs" in n
-        kern[n] = _kernel_entry(flops[n], per[n], pk["bf16"] if dl else fp8_peak,
-                                "bf16" if dl else "fp8 (2x measured bf16)", alg_bytes[n], pk["hbm"])
+        kern[n] = _kernel_entry(flops[n], per[n], bf_peak if dl else fp8_peak,
+                                f"bf16 {peak_kind}" if dl else f"fp8 (2x measured bf16 {peak_kind})",
+                                alg_bytes[n], pk["hbm"])
 
     # ----------------------------------------------- extra: BF16 arm, dequant
     extra = {}
@@ -806,18 +813,22 @@ def main():
             # its larger launch is the wi dLHS
             "roofline": {"kernel": "wi dLHS (gmm_dlhs_pair_kernel: CTA pairs, dequantized weight in TMEM)",
                          "bound": "tensor", "achieved": round(dl_tflops, 1),
-                         "peak": round(pk["bf16"], 1), "unit": "TFLOP/s",
-                         "frac": round(dl_tflops / pk["bf16"], 3),
+                         "peak": round(bf_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(dl_tflops / bf_peak, 3),
+                         "frac_of_burst": round(dl_tflops / pk["bf16"], 3),
                          "traffic": tr_dl if E == 32 else None,
                          "traffic_source": tr_dl_why if E == 32 else "other workload",
-                         "peak_source": f"{pk['source']} bf16, burst"},
+                         "peak_source": f"{pk['source']} bf16, {peak_kind} "
+                                        f"(timed region {ms_total / 1e3:.2f} s)"},
             # the row the pages' target is set on: the wi forward with its quantization
             "roofline_wi_fwd": {"kernel": "wi fwd (row quantize + FP8 GMM + SwiGLU)", "bound": "tensor",
                                 "achieved": round(wi_tflops, 1), "peak": round(fp8_peak, 1),
                                 "unit": "TFLOP/s", "frac": round(wi_tflops / fp8_peak, 3),
+                                "frac_of_burst": round(wi_tflops / (2.0 * pk["bf16"]), 3),
                                 "traffic": tr_fw if E == 32 else None,
                                 "traffic_source": tr_fw_why if E == 32 else "other workload",
-                                "peak_source": f"{pk['source']} bf16 x2 (fp8/bf16 nominal ratio), burst"},
+                                "peak_source": f"{pk['source']} bf16 x2 (fp8/bf16 nominal ratio), "
+                                               f"{peak_kind}"},
             "kernels": kern, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, **extra,
         }
         print(json.dumps(line), flush=True)
