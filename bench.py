@@ -48,12 +48,12 @@ METRIC = "FP8 GMM TFLOP/s (wi+SwiGLU fwd, wo fwd, dLHS) and % of GB300 FP8 peak"
 CSRC = os.path.join(ROOT, "fp8_moe_routed_gb300", "csrc")
 TRAFFIC = {
     # row quantizer + wi GMM (E=32 x 1024 rows, K=7168, N=4096):
-    # quantize_rows_kernel<4> 469.8 + 202.4 MB, gmm_fwd_kernel<1, 1, 0> 1511.4 + 125.7 MB
-    "wi_fwd": {"bytes": 2309.4e6, "sha1": "720c3287ff2eee6de9b6e28fc91a4bf84682699f",
+    # quantize_rows_kernel<4> 469.8 + 201.8 MB, gmm_fwd_kernel<1, 1, 0> 1197.5 + 125.0 MB
+    "wi_fwd": {"bytes": 1994.1e6, "sha1": "86259e5da9c609346240b48c95c5ecc155a33b4d",
                "sources": ("quant.cu", "quantize.cuh", "gmm_fwd.cu", "ptx.cuh", "groups.cuh")},
     # the wi dLHS launch (contraction 4096, output 7168): gmm_dlhs_pair_kernel<0>
-    # 1351.0 + 458.4 MB
-    "wi_dlhs": {"bytes": 1809.4e6, "sha1": "3b5ad397756f8b5531e06af4cb28faa31b63b8ef",
+    # 1353.6 + 458.1 MB
+    "wi_dlhs": {"bytes": 1811.7e6, "sha1": "3b511c56baa262bb93d1712526577d73e67bccaa",
                 "sources": ("gmm_dlhs_pair.cu", "ptx.cuh", "groups.cuh")},
 }
 

@@ -1,7 +1,6 @@
-// quantize.cuh -- the activation quantization arithmetic shared by the
-// quantizer kernels (quant.cu) and the forward GMM's in-kernel row quantizer
-// (gmm_fwd.cu): scale = max(amax, 1e-12) / fmt_max by IEEE division, codes of
-// the correctly rounded f32 quotient x / scale ("MoE: native FP8 QAT for
+// quantize.cuh -- the activation quantization arithmetic of the quantizer
+// kernels (quant.cu): scale = max(amax, 1e-12) / fmt_max by IEEE division, codes
+// of the correctly rounded f32 quotient x / scale ("MoE: native FP8 QAT for
 // routed-expert GMMs", Implementation: per-row full-K f32 scale).
 #pragma once
 #include <cstdint>
@@ -64,17 +63,43 @@ __device__ __forceinline__ void bracket(float s, float& rl, float& rh) {
   rh = __fmul_rn(r, 1.0f + 0x1p-20f);
 }
 
-// 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2).
+// 8 bf16 (one uint4) / s -> 8 e4m3 codes (one uint2). The bracket products of
+// all four pairs are converted first; only when some pair's two codes differ
+// (about once in 2^16 values) are the exact IEEE quotients of the eight values
+// converted instead, so the common case takes one test and one branch per eight
+// values (row quantizer: K = 7168 122.0 -> 120.5 us, K = 2048 39.1 -> 37.3 us at
+// 32768 rows; the per-column tile quantizer measured slower this way and keeps
+// quotient_x2).
 __device__ __forceinline__ uint2 quant8(uint4 v, float s, float rl, float rh) {
-  uint2 o;
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint16_t c[4];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t lo[2], hi[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    c[i] = quotient_x2<false>(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), s, s, rl, rl, rh, rh);
-  o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
-  o.y = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
-  return o;
+  for (int i = 0; i < 2; ++i) {
+    uint16_t cl[2], ch[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float x0 = bf16lo_to_f32(w[2 * i + j]), x1 = bf16hi_to_f32(w[2 * i + j]);
+      float pl0, pl1, ph0, ph1;
+      mul_f32x2(x0, x1, rl, rl, pl0, pl1);
+      mul_f32x2(x0, x1, rh, rh, ph0, ph1);
+      cl[j] = f32x2_to_e4m3x2(pl0, pl1);
+      ch[j] = f32x2_to_e4m3x2(ph0, ph1);
+    }
+    lo[i] = (uint32_t)cl[0] | ((uint32_t)cl[1] << 16);
+    hi[i] = (uint32_t)ch[0] | ((uint32_t)ch[1] << 16);
+  }
+  if ((lo[0] ^ hi[0]) | (lo[1] ^ hi[1])) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint16_t c[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        c[j] = f32x2_to_e4m3x2(__fdiv_rn(bf16lo_to_f32(w[2 * i + j]), s),
+                               __fdiv_rn(bf16hi_to_f32(w[2 * i + j]), s));
+      lo[i] = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+    }
+  }
+  return make_uint2(lo[0], lo[1]);
 }
 
 }  // namespace fp8moe

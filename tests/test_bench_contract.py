@@ -97,3 +97,12 @@ def test_traffic_is_null_unless_captured_on_the_current_sources(monkeypatch):
     monkeypatch.setitem(bench.TRAFFIC, "wi_dlhs", dict(t, bytes=1.5e9, sha1="0" * 40))
     b, why = bench.traffic("wi_dlhs")
     assert b is None and "changed" in why
+
+
+def test_committed_traffic_figures_match_the_committed_sources():
+    """Each traffic figure in bench.py was captured on the kernel sources as
+    committed: a kernel change must come with a new capture."""
+    import bench
+    for kind in bench.TRAFFIC:
+        b, why = bench.traffic(kind)
+        assert b is not None, f"{kind}: {why}"
