@@ -43,6 +43,7 @@ EXPORTS = [
     "fp8moe_gmm_dlhs_dswiglu_fp8", "fp8moe_gmm_dlhs_dswiglu_fp8_path",
     "fp8moe_tgmm_drhs_quant_fmt", "fp8moe_tgmm_quantize_tiles_fmt",
     "fp8moe_gmm_fp8_fwd_block", "fp8moe_quantize_rows_block", "fp8moe_selftest_wait_timeout",
+    "fp8moe_selftest_cast_f32",
 ]
 
 FMT = {"e4m3": 0, "e5m2": 1}
@@ -98,6 +99,7 @@ def load(build_if_missing: bool = True):
                                          I32),
             "fp8moe_quantize_rows_block": ([P, I64, I64, P, I32, I32, P, P, P], I32),
             "fp8moe_selftest_wait_timeout": ([ctypes.c_uint32, P], I32),
+            "fp8moe_selftest_cast_f32": ([P, I64, I32, P, P], I32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -412,6 +414,17 @@ def selftest_wait_timeout(limit_us: int, device=None) -> None:
     """Enqueue the bounded-wait failure self-test (see fp8moe_selftest_wait_timeout)."""
     _check(load().fp8moe_selftest_wait_timeout(int(limit_us), _stream(device)),
            "fp8moe_selftest_wait_timeout")
+
+
+def selftest_cast_f32(x, fmt: str = "e4m3", codes=None):
+    """The quantizers' f32 -> fp8 cast on arbitrary f32 values (a device tensor):
+    codes u8 of x's shape (see fp8moe_selftest_cast_f32)."""
+    _req(x, torch.float32, "x", x.dim())
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(load().fp8moe_selftest_cast_f32(_ptr(x), x.numel(), FMT[fmt], _ptr(codes),
+                                           _stream(x.device)), "fp8moe_selftest_cast_f32")
+    return codes
 
 
 def read_status(device=None) -> int:

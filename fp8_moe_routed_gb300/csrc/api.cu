@@ -609,6 +609,20 @@ int fp8moe_selftest_wait_timeout(uint32_t limit_us, fp8moe_stream_t stream) {
   return FP8MOE_OK;
 }
 
+int fp8moe_selftest_cast_f32(const float* x, int64_t n, int32_t fmt, uint8_t* codes,
+                             fp8moe_stream_t stream) {
+  if (n < 0 || (fmt != FP8MOE_FMT_E4M3 && fmt != FP8MOE_FMT_E5M2)) return FP8MOE_EINVAL;
+  if (n == 0) return FP8MOE_OK;
+  if (!x || !codes) return FP8MOE_EINVAL;
+  if (reinterpret_cast<uintptr_t>(x) & 3u) return FP8MOE_EALIGN;
+  int sms = 0;
+  int rc = device_init(&sms);
+  if (rc) return rc;
+  cudaError_t e = fp8moe_launch_selftest_cast(x, n, fmt, codes, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FP8MOE_OK;
+}
+
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags) {
   if (!flags) return FP8MOE_EINVAL;
   uint32_t v = 0;

@@ -88,3 +88,7 @@ uint32_t fp8moe_status_take_selftest(cudaStream_t s);
 // One thread waits on an mbarrier that nothing completes for limit_ns, then
 // records a wait timeout (selftest.cu).
 cudaError_t fp8moe_launch_selftest_wait(uint64_t limit_ns, cudaStream_t s);
+// Converts n f32 values to fp8 codes (fmt 0 e4m3, 1 e5m2) with the quantizers'
+// cast (selftest.cu).
+cudaError_t fp8moe_launch_selftest_cast(const float* x, int64_t n, int fmt, uint8_t* out,
+                                        int num_sms, cudaStream_t s);

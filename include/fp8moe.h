@@ -246,6 +246,20 @@ int fp8moe_tgmm_quantize_tiles_fmt(const void* lhs, const void* dout, int64_t M,
  * has no counterpart. */
 int fp8moe_selftest_wait_timeout(uint32_t limit_us, fp8moe_stream_t stream);
 
+/* The f32 -> fp8 cast that every quantizer of the library ends in, on
+ * arbitrary inputs: codes[i] = RN_sat(x[i]) in the format fmt (FP8MOE_FMT_E4M3:
+ * round to nearest even, saturating at +-448, NaN -> NaN code; FP8MOE_FMT_E5M2:
+ * the same at +-57344), converted two values at a time by the same
+ * cvt.rn.satfinite helpers as the quantizers ("MoE: native FP8 QAT for
+ * routed-expert GMMs", Implementation: the e4m3 activation codes; "MoE fp8
+ * backward: in-kernel drhs operand quantization", What: the e5m2 gradient
+ * codes).  x f32 [n] and codes u8 [n] are device pointers, x 4-byte aligned;
+ * the caller owns both.  n = 0 does nothing.  FP8MOE_EINVAL: n < 0, an unknown
+ * fmt, or a null pointer with n > 0.  For parity tests of the cast over whole
+ * binades of bit patterns. */
+int fp8moe_selftest_cast_f32(const float* x, int64_t n, int32_t fmt, uint8_t* codes,
+                             fp8moe_stream_t stream);
+
 /* Waits for `stream`, returns in *flags the OR of the FP8MOE_STATUS_* bits set
  * since the last call, and clears them. */
 int fp8moe_read_status(fp8moe_stream_t stream, uint32_t* flags);

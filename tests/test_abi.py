@@ -67,6 +67,11 @@ def test_argument_checks_run_before_any_device_call():
     # argument checks of the entry points added for the next steps of the path
     assert L.fp8moe_selftest_wait_timeout(0, None) == -1              # limit must be > 0
     assert L.fp8moe_selftest_wait_timeout(3000000, None) == -1        # and <= 2 s
+    assert L.fp8moe_selftest_cast_f32(P(16), -1, 0, P(16), None) == -1  # n >= 0
+    assert L.fp8moe_selftest_cast_f32(P(16), 8, 7, P(16), None) == -1   # unknown format
+    assert L.fp8moe_selftest_cast_f32(None, 8, 0, P(16), None) == -1    # null input
+    assert L.fp8moe_selftest_cast_f32(P(18), 8, 1, P(16), None) == -2   # x not 4-byte aligned
+    assert L.fp8moe_selftest_cast_f32(None, 0, 0, None, None) == 0      # empty: nothing to do
     assert L.fp8moe_gmm_fp8_fwd_block(P(16), 128, 512, P(16), P(16), 2, 256, P(16), P(16),
                                       P(256), 10 ** 9, 256, 0, None) == -1   # block must be 512
     assert L.fp8moe_tgmm_drhs_quant_fmt(P(16), P(16), 128, 64, 64, 1, P(16), P(16), P(256),
