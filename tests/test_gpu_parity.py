@@ -88,6 +88,7 @@ FWD_CASES = [
     (700, 512, 512, 5, [300, 0, 129, 1, 200]),      # T=630 < M: ragged tail
     (384, 1024, 768, 3, [0, 384, 0]),               # one group owns everything
     (256, 256, 352, 2, [100, 100]),                 # N not a multiple of 256 (silu: 176)
+    (300, 336, 224, 3, [120, 0, 150]),              # K not a multiple of the 128-wide k step
 ]
 
 
